@@ -1,0 +1,436 @@
+#!/usr/bin/env python
+"""Throughput of one Nexus Sampling eviction step (scores, walk, reservoir selection,
+in-place compaction) on the GB300, through the library's C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+                    [--workload llama3_8b_layer]
+
+One step = nexus_evict_step over every slice of the workload's step-0 cache (for the
+default workload: one Llama-3-8B-shaped layer, 8 KV heads x 8192 cached rows, evicted
+to 1638 rows each). Before each timed step, untimed: the cache is restored from a
+pristine device copy and a buffer twice the L2 size is written, so every step reads
+the cache from HBM. Rank 0 prints one JSON line.
+
+value   KV rows scored+evicted per second (a row = one cached token of one KV head of
+        one layer), all ranks, device-timed with CUDA events on the launching stream.
+e2e     the same metric end to end through the C ABI with host buffers: per step the
+        cache, queries and lengths are copied from pinned host memory to the device,
+        the step runs, and the kept-slot lists and lengths are copied back.
+roofline  the dominant kernel: algorithmic bytes per launch / its mean event-timed
+        duration, against the measured HBM copy bandwidth.
+cpu_baseline  the CPU oracle (C, OpenMP over slices) on the host cores, bounded sample.
+--impl reference  runs the CPU oracle itself as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "cached tokens scored+evicted/s per eviction step; % HBM roofline (1×GB300)"
+UNIT = "KV rows/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("native", "reference"), default="native")
+    ap.add_argument("--workload", default="llama3_8b_layer")
+    ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=float(d["hbm_gbs"]), src="measured")
+    return dict(hbm_gbs=FALLBACK_HBM_GBS, src="fallback")
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="nx_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["nvidia-smi unavailable"])
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["no samples"])
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1])]
+        mx = [num(r[2]) for r in rows if num(r[2])]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return dict(sm_mhz=statistics.median(sm) if sm else None,
+                    sm_max_mhz=max(mx) if mx else None, reasons=reasons, samples=len(rows),
+                    power_w_max=max((num(r[3]) or 0) for r in rows))
+
+
+# ---------------------------------------------------------------------------
+# distributed (one process per GPU; host-side barrier and max only)
+# ---------------------------------------------------------------------------
+
+def dist_setup(gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allmax(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes (what the method must move)
+# ---------------------------------------------------------------------------
+
+def algorithmic_bytes(wl, lens0: np.ndarray, keep: np.ndarray, newlen: np.ndarray) -> dict:
+    """Per step: K read once + pos (scoring), queries, the kept-slot list, and every
+    moved row's k, v and pos read and written (compaction)."""
+    eb = 2 if wl.dtype == "bf16" else 4
+    row = wl.head_dim * eb
+    rows = int(lens0.sum())
+    moved = 0
+    for i in range(keep.shape[0]):
+        n = int(newlen[i])
+        moved += int((keep[i, :n] != np.arange(n)).sum())
+    qbytes = wl.n_slices * wl.group * wl.window * wl.head_dim * eb
+    score = rows * (row + 4) + qbytes
+    compact = moved * (4 * row + 8) + int(newlen.sum()) * 4
+    return dict(rows=rows, moved=moved, score=score, compact=compact, total=score + compact)
+
+
+# ---------------------------------------------------------------------------
+# native arm
+# ---------------------------------------------------------------------------
+
+def run_native(args, rank, world, local):
+    from streaming_kv_cache_step_gb300 import nexus
+    from streaming_kv_cache_step_gb300 import workloads as W
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = W.WORKLOADS[args.workload]()
+    pristine = W.make_cache(wl, dev)
+    work = {k: (v.clone() if torch.is_tensor(v) else v) for k, v in pristine.items()}
+    q = W.queries(wl, 0, dev)
+    cache = nexus.Cache.from_dict(work)
+    params = nexus.Params(budget=work["budget"], budget_max=int(wl.budget.max()),
+                          window=wl.window, walk_len=wl.walk_len, n_sink=wl.n_sink,
+                          n_recent=wl.n_recent, lam=wl.lam, eps_tie=wl.eps_tie,
+                          seed=wl.philox_seed, step=0, seq_id_base=rank * wl.seqs)
+    ws = nexus.alloc_workspace(cache, params)
+    status = nexus.new_status(dev)
+    keep = torch.full((cache.n_slices, wl.capacity), -1, dtype=torch.int32, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    names = ("k", "v", "pos", "lens")
+
+    def restore():
+        for n in names:
+            work[n].copy_(pristine[n], non_blocking=True)
+        flush.zero_()
+
+    def step(events=None):
+        arr = nexus.profile_next_call(events) if events else None
+        nexus.evict_step(cache, q, params, keep, ws, status)
+        del arr
+
+    for _ in range(args.warmup):
+        restore()
+        step()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    launch_names = nexus.last_launch_names()
+    nl = len(launch_names)
+
+    # ---- timed region ----
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(nl)] for _ in range(K)]
+    launches = 0
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(K):
+        restore()
+        starts[i].record(stream)
+        step(kev[i])
+        ends[i].record(stream)
+        launches += nexus.last_launch_count()
+    torch.cuda.synchronize()
+    barrier(world)
+    time.sleep(0.2)
+    clocks = sampler.stop()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+
+    step_ms = [starts[i].elapsed_time(ends[i]) for i in range(K)]
+    total_ms = allmax(sum(step_ms), world)
+    per_kernel = {}
+    for j, name in enumerate(launch_names):
+        t = []
+        for i in range(K):
+            prev = starts[i] if j == 0 else kev[i][j - 1]
+            t.append(prev.elapsed_time(kev[i][j]))
+        per_kernel[f"{j}:{name}"] = statistics.mean(t) * 1e3   # microseconds
+
+    # algorithmic bytes of this step (from the kept-slot lists of the last step)
+    lens0 = pristine["lens"].reshape(-1).cpu().numpy()
+    newlen = work["lens"].reshape(-1).cpu().numpy()
+    ab = algorithmic_bytes(wl, lens0, keep.cpu().numpy(), newlen)
+    rows_per_step = ab["rows"]
+    value = rows_per_step * K * world / (total_ms / 1e3)
+
+    # dominant kernel and its roofline
+    dom = max(per_kernel, key=per_kernel.get)
+    dom_name = dom.split(":", 1)[1]
+    if "compact" in dom_name:
+        dom_bytes = ab["compact"]
+    elif "select" in dom_name:
+        dom_bytes = rows_per_step * 4 + int(newlen.sum()) * 4
+    else:
+        dom_bytes = ab["score"]
+    peaks = measured_peaks()
+    achieved = dom_bytes / (per_kernel[dom] * 1e-6) / 1e9
+    step_gbs = ab["total"] / (statistics.mean(step_ms) * 1e-3) / 1e9
+    roofline = dict(bound="hbm", kernel=dom_name, achieved=round(achieved, 1),
+                    peak=peaks["hbm_gbs"], unit="GB/s",
+                    frac=round(achieved / peaks["hbm_gbs"], 4), traffic=None,
+                    peak_source=peaks["src"],
+                    whole_step=dict(achieved=round(step_gbs, 1),
+                                    frac=round(step_gbs / peaks["hbm_gbs"], 4),
+                                    alg_bytes=ab["total"]))
+
+    # ---- end to end through the C ABI with host buffers ----
+    e2e_steps = args.e2e_steps or max(3, min(K, 50))
+    host = {n: torch.empty_like(pristine[n], device="cpu").pin_memory() for n in names}
+    for n in names:
+        host[n].copy_(pristine[n])
+    q_host = torch.empty_like(q, device="cpu").pin_memory()
+    q_host.copy_(q)
+    keep_host = torch.empty_like(keep, device="cpu").pin_memory()
+    lens_host = torch.empty_like(pristine["lens"], device="cpu").pin_memory()
+    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    h2d = sum(host[n].numel() * host[n].element_size() for n in names) + \
+        q_host.numel() * q_host.element_size()
+    d2h = keep_host.numel() * 4 + lens_host.numel() * 4
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(e2e_steps):
+        flush.zero_()
+        e_s[i].record(stream)
+        for n in names:
+            work[n].copy_(host[n], non_blocking=True)
+        q.copy_(q_host, non_blocking=True)
+        nexus.evict_step(cache, q, params, keep, ws, status)
+        keep_host.copy_(keep, non_blocking=True)
+        lens_host.copy_(work["lens"], non_blocking=True)
+        e_e[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = allmax(sum(e_s[i].elapsed_time(e_e[i]) for i in range(e2e_steps)), world)
+    e2e_value = rows_per_step * e2e_steps * world / (e2e_ms / 1e3)
+
+    out = dict(metric=METRIC, value=round(value, 1), unit=UNIT, n_gpus=world, steps=K,
+               warmup=args.warmup, ms_per_step=round(total_ms / K, 5), higher_is_better=True,
+               scaling="weak", vs_baseline=None, dtype=wl.dtype, data="synthetic",
+               config=dict(workload=wl.name, layers=wl.layers, seqs=wl.seqs,
+                           q_heads=wl.q_heads, kv_heads=wl.kv_heads, head_dim=wl.head_dim,
+                           cache_rows=int(wl.lens.max()), budget=int(wl.budget.max()),
+                           window=wl.window, walk=wl.walk_len, n_sink=wl.n_sink,
+                           n_recent=wl.n_recent, rows_per_step=rows_per_step,
+                           moved_rows=ab["moved"], alg_bytes_per_step=ab["total"],
+                           l2="flushed between timed steps (2x L2 written)",
+                           parallelism=f"dp{world} (independent sequences per rank)"),
+               roofline=roofline,
+               e2e=dict(value=round(e2e_value, 1), unit=UNIT, h2d_bytes_per_step=h2d,
+                        d2h_bytes_per_step=d2h, steps=e2e_steps),
+               gpu_launches=launches, kernels_us={k: round(v, 3) for k, v in per_kernel.items()},
+               clocks=clocks)
+    return out, wl
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (cpu_baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+
+def _oracle_slices(wl, max_slices):
+    from streaming_kv_cache_step_gb300 import workloads as W
+    return [W.slice_numpy_cache(wl, sid) for sid in range(min(wl.n_slices, max_slices))]
+
+
+def _oracle_pass(wl, slices, pool):
+    """One pass of the oracle's eviction step over the sampled slices, one host thread
+    per slice (ctypes releases the GIL); returns the rows processed."""
+    import oracle
+
+    def run_slice(item):
+        c, q, over = item
+        cc = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in c.items()}
+        pr = dict(window=wl.window, walk_len=wl.walk_len, n_sink=wl.n_sink,
+                  n_recent=wl.n_recent, lam=wl.lam, eps_tie=wl.eps_tie, seed=wl.philox_seed,
+                  step=0, **over)
+        oracle.evict_step(cc, q, pr, mutate=True, nthreads=1)
+        return int(c["lens"].reshape(-1)[0])
+
+    return sum(pool.map(run_slice, slices))
+
+
+def oracle_rate(wl, budget_s: float):
+    """cpu_baseline: rows/s of the CPU oracle, wall-clock, on a bounded sample."""
+    from concurrent.futures import ThreadPoolExecutor
+    import oracle
+    oracle.build()
+    cores = os.cpu_count() or 1
+    slices = _oracle_slices(wl, cores)
+    rows, passes = 0, 0
+    with ThreadPoolExecutor(max_workers=len(slices)) as pool:
+        t0 = time.perf_counter()
+        while True:
+            rows += _oracle_pass(wl, slices, pool)
+            passes += 1
+            dt = time.perf_counter() - t0
+            if dt >= budget_s:
+                break
+    return dict(value=round(rows / dt, 1), unit=UNIT, cores=len(slices), kind="oracle",
+                sample=f"{passes} passes over {len(slices)} of the {wl.n_slices} step-0 slices "
+                       f"of {wl.name} ({rows} rows, {dt:.1f} s wall), one host thread per slice")
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the CPU oracle as it stands, K timed steps after W warm-up steps,
+    each step one pass over a bounded sample of the workload's slices."""
+    from concurrent.futures import ThreadPoolExecutor
+    from streaming_kv_cache_step_gb300 import workloads as W
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    wl = W.WORKLOADS[args.workload]()
+    slices = _oracle_slices(wl, os.cpu_count() or 1)
+    with ThreadPoolExecutor(max_workers=len(slices)) as pool:
+        for _ in range(args.warmup):
+            _oracle_pass(wl, slices, pool)
+        t0 = time.perf_counter()
+        rows = 0
+        for _ in range(args.steps):
+            rows += _oracle_pass(wl, slices, pool)
+        dt = time.perf_counter() - t0
+    value = rows / dt
+    sample = (f"{len(slices)} of the {wl.n_slices} step-0 slices of {wl.name} per step, "
+              f"one host thread per slice")
+    return dict(metric=METRIC, value=round(value, 1), unit=UNIT, n_gpus=world,
+                steps=args.steps, warmup=args.warmup,
+                ms_per_step=round(dt / max(args.steps, 1) * 1e3, 3), higher_is_better=True,
+                scaling="weak", vs_baseline=None, dtype="f64", data="synthetic",
+                impl="reference",
+                config=dict(workload=wl.name, sample_slices=len(slices),
+                            rows_per_step=rows // max(args.steps, 1)),
+                cpu_baseline=dict(value=round(value, 1), unit=UNIT, cores=len(slices),
+                                  kind="oracle", sample=sample),
+                e2e=dict(value=round(value, 1), unit=UNIT, h2d_bytes_per_step=0,
+                         d2h_bytes_per_step=0))
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    out, wl = run_native(args, rank, world, local)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            out["cpu_baseline"] = oracle_rate(wl, budget_s=10.0)
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

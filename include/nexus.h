@@ -1,0 +1,219 @@
+/*
+ * nexus.h -- C ABI of the GB300 (sm_103a) per-step eviction library (libnexus.so).
+ *
+ * The library implements one eviction step of Nexus Sampling as defined in
+ * "Forget Without Compromise: Nexus Sampling for Streaming KV-Cache Eviction Under
+ * Fixed Budgets": direct scores (§2.1 Eq. (1), §2.2 Eq. (3)), the Nexus walk and
+ * weight (§2.2 Eqs. (2), (4), (5)), weighted reservoir selection of B survivors
+ * (§2.3 Eq. (6) with n = 1, i.e. Efraimidis-Spirakis keys ln(u)/w), and the
+ * in-place compaction that lets inference continue with K_S, V_S (§2.1,
+ * "streaming view").
+ *
+ * Terms
+ *   slice   one (layer l, sequence s, KV head h); slices are independent.
+ *           slice id = (l * seqs + s) * kv_heads + h.
+ *   row     one cached (key, value) of one slice; slot j = its index 0..T-1.
+ *   T       rows currently cached in a slice (lens[slice]).
+ *   B       the budget: rows kept per slice of sequence s (budget[s]).
+ *   W, H    window rows and walk length; G = query heads per KV head.
+ *
+ * Conventions (every entry point)
+ *   - All buffer pointers are DEVICE pointers owned by the caller. The library
+ *     never allocates, frees or synchronises; scratch memory is the caller's
+ *     workspace of nexus_workspace_bytes() bytes (256-byte aligned).
+ *   - Calls are asynchronous on `stream`. The returned nx_status covers argument
+ *     checks and launch errors only. Conditions found on the device are OR-ed into
+ *     *dev_status (an int32 in device memory, caller-owned, which the caller zeroes
+ *     and reads after synchronising): NX_DEV_* bits below.
+ *   - Calls on different streams are independent when their workspaces and
+ *     outputs are disjoint. Two calls must not share a workspace concurrently.
+ *   - Block granularity is b = 1 (one decision per token).
+ */
+#ifndef NEXUS_H_
+#define NEXUS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL means the legacy default stream. */
+typedef struct CUstream_st* nx_stream_t;
+
+typedef enum nx_status {
+  NX_OK = 0,
+  NX_ERR_INVALID_ARG = 1,   /* a size, pointer, alignment or parameter is out of range */
+  NX_ERR_UNSUPPORTED = 2,   /* valid for the method, not built here (n_avg > 1)        */
+  NX_ERR_CUDA = 3,          /* a CUDA launch or memset failed                           */
+  NX_ERR_TIMEOUT = 4,       /* reserved: device waits report through dev_status         */
+  NX_ERR_WORKSPACE = 5,     /* ws is NULL, misaligned or smaller than required          */
+  NX_ERR_DEVICE_FAULT = 6   /* reserved                                                 */
+} nx_status;
+
+/* Bits OR-ed into *dev_status by the device. */
+enum {
+  NX_DEV_TIMEOUT = 1,       /* a bounded wait between thread blocks gave up; outputs of
+                               the affected call are incomplete (the cache may be
+                               partially compacted) */
+  NX_DEV_BAD_LEN = 2,       /* lens[slice] < 0 or > capacity: slice left untouched */
+  NX_DEV_BAD_BUDGET = 4,    /* budget[s] < n_sink + n_recent or > budget_max: untouched */
+  NX_DEV_BAD_PAGE = 8       /* a block_table entry is outside [0, num_pages): untouched */
+};
+
+enum { NX_DTYPE_F32 = 0, NX_DTYPE_BF16 = 1 };
+enum { NX_MODE_RESERVOIR = 0, NX_MODE_TOPK = 1 };
+
+/*
+ * The KV cache. Two layouts:
+ *   contiguous (page_size == 0): k, v [layers][seqs][kv_heads][capacity][head_dim],
+ *                                pos    [layers][seqs][kv_heads][capacity];
+ *   paged (page_size > 0):       k, v [layers][num_pages][kv_heads][page_size][head_dim],
+ *                                pos    [layers][num_pages][kv_heads][page_size];
+ *     slot j of (l, s, h) lives in page block_table[s * max_pages_per_seq + j / page_size]
+ *     at row j % page_size; capacity = max_pages_per_seq * page_size.
+ * lens [layers][seqs][kv_heads] int32: rows cached per slice (read, then set to
+ * min(T, B) by kv_compact / nexus_evict_step). pos holds each row's absolute token
+ * position (the token index of the Philox counter); it moves with its row.
+ */
+typedef struct nx_cache {
+  int32_t layers, seqs, kv_heads;
+  int32_t group;               /* G: query heads per KV head (GQA) */
+  int32_t head_dim;            /* 64 or 128 */
+  int32_t capacity;            /* rows per slice */
+  int32_t page_size;           /* 0 (contiguous) or 8, 16, 32, 64, 128 */
+  int32_t num_pages;           /* paged: pages per layer */
+  int32_t max_pages_per_seq;   /* paged: columns of block_table */
+  int32_t dtype;               /* NX_DTYPE_BF16 or NX_DTYPE_F32, for k, v and the queries */
+  void* k;                     /* 16-byte aligned */
+  void* v;                     /* 16-byte aligned */
+  int32_t* pos;
+  int32_t* lens;
+  const int32_t* block_table;  /* paged only, [seqs][max_pages_per_seq] */
+} nx_cache;
+
+/*
+ * Step parameters. Defaults from the paper's implementation details (§5.1):
+ * lambda = 0.5, eps_tie = 1e-6; the paper's W = 16, H = 3. n_sink / n_recent are the
+ * forced attention-sink and recency slots of §2.3 (counted inside B; 32 each is the
+ * default reading, one paper block each).
+ */
+typedef struct nx_params {
+  int32_t window;              /* W, 1..64 */
+  int32_t walk_len;            /* H, 0..min(W, 8): the last H window rows, oldest first */
+  int32_t n_sink;              /* first n_sink slots always kept */
+  int32_t n_recent;            /* last n_recent slots always kept */
+  int32_t n_avg;               /* reservoir averaging count n of Eq. (6); must be 1 */
+  int32_t mode;                /* NX_MODE_RESERVOIR, or NX_MODE_TOPK (keep the top by w) */
+  float lambda;                /* mixing weight of Eq. (2), >= 0 */
+  float eps_tie;               /* recency tie-break of Eq. (5), >= 0 */
+  const int32_t* budget;       /* device int32 [seqs]: B per sequence */
+  int32_t budget_max;          /* host bound: every budget[s] <= budget_max <= capacity */
+  int32_t seq_id_base;         /* Philox sequence id of s is seq_id_base + s (< 2^24) */
+  int32_t layer_id_base;       /* Philox head id of (l, h) is (layer_id_base + l) * kv_heads + h */
+  uint32_t step;               /* Philox step id; callers advance it per eviction step */
+  uint64_t seed;               /* Philox key */
+} nx_params;
+
+/*
+ * Bytes of workspace every entry point below needs for these arguments (0 on
+ * invalid arguments). One workspace may serve all five calls in turn.
+ */
+size_t nexus_workspace_bytes(const nx_cache* cache, const nx_params* params);
+
+/*
+ * Direct scores, §2.1 Eq. (1) at b = 1 and §2.2 Eq. (3):
+ *   Qbar_w = (1/G) sum_g q[g][w];  P_w = softmax_j(Qbar_w . k_j / sqrt(head_dim)) over
+ *   the whole cache (no mask);     a_j = (1/W) sum_w P_w[j].
+ * q: [layers][seqs][kv_heads * group][window][head_dim] in cache->dtype (device,
+ *    16-byte aligned); query head kv_head * group + g belongs to KV head kv_head.
+ * a_out: float [slices][capacity], entries j < T written.
+ * row_stats_out (nullable): float [slices][window][2] = (max_j logit, sum_j exp(logit - max)).
+ * Errors: NX_ERR_INVALID_ARG, NX_ERR_WORKSPACE, NX_ERR_CUDA. Empty slices (T = 0)
+ * write nothing.
+ */
+nx_status nexus_direct_scores(const nx_cache* cache, const void* q, const nx_params* params,
+                              float* a_out, float* row_stats_out, void* ws, size_t ws_bytes,
+                              int32_t* dev_status, nx_stream_t stream);
+
+/*
+ * Nexus weight, §2.2 Eqs. (4), (2), (5):
+ *   C = 0; for the last H window rows q, oldest first: gamma_q = 1 + <P_q, C>,
+ *   C += gamma_q P_q;  c~ = C / ||C||_1 (0 when H = 0);  s = a + lambda c~;
+ *   w_j = s_j + eps_tie * j / (T - 1)  (the ramp is 0 when T = 1).
+ * Computes everything from the cache and q (same layout as nexus_direct_scores).
+ * w_out: float [slices][capacity]; ctilde_out (nullable): float [slices][capacity].
+ */
+nx_status nexus_walk(const nx_cache* cache, const void* q, const nx_params* params, float* w_out,
+                     float* ctilde_out, void* ws, size_t ws_bytes, int32_t* dev_status,
+                     nx_stream_t stream);
+
+/*
+ * Weighted reservoir selection, §2.3 and Eq. (6) with n = 1 (Efraimidis-Spirakis):
+ *   forced F = slots [0, n_sink) and [T - n_recent, T); K = B - |F|;
+ *   for j not in F: x = word 0 of Philox4x32-10(counter = (pos_j, step, head id,
+ *   seq id), key = seed), u = (2 (x >> 9) + 1) 2^-24, kappa_j = ln(u) / w_j in
+ *   binary32 (ln by the library's specified binary32 logarithm, IEEE division);
+ *   keep the K largest (kappa desc, then slot desc) -- in NX_MODE_TOPK kappa_j = w_j.
+ * w: float [slices][capacity] (device). keep_idx: int32 [slices][capacity]: the first
+ * min(T, B) entries receive the kept slots in ascending order (0..T-1 when T <= B);
+ * the rest are not written. The cache is read (lens, pos), not modified.
+ */
+nx_status nexus_reservoir_select(const float* w, const nx_cache* cache, const nx_params* params,
+                                 int32_t* keep_idx, void* ws, size_t ws_bytes,
+                                 int32_t* dev_status, nx_stream_t stream);
+
+/*
+ * In-place compaction (§2.1: inference continues with K_S, V_S): for every slice with
+ * n = min(T, B) and i < n, row i <- row keep_idx[i] (k, v and pos), then lens = n.
+ * keep_idx: int32 [slices][capacity], ascending, as written by nexus_reservoir_select.
+ * Rows at or beyond n and the block table are not modified; rows with
+ * keep_idx[i] == i are not rewritten. Uses the workspace for tile flags; bounded
+ * waits report NX_DEV_TIMEOUT.
+ */
+nx_status kv_compact(nx_cache* cache, const int32_t* keep_idx, const nx_params* params,
+                     void* ws, size_t ws_bytes, int32_t* dev_status, nx_stream_t stream);
+
+/*
+ * One whole eviction step: scores, walk, reservoir selection and compaction for every
+ * slice, with the same results as the four calls above in sequence.
+ * keep_idx_out (nullable): int32 [slices][capacity] receives the kept slots.
+ */
+nx_status nexus_evict_step(nx_cache* cache, const void* q, const nx_params* params,
+                           int32_t* keep_idx_out, void* ws, size_t ws_bytes,
+                           int32_t* dev_status, nx_stream_t stream);
+
+/*
+ * Testing hook for failure detection (not part of the method): kv_compact, except that
+ * compaction tile number skip_signal_tile (slice * tiles_per_slice + tile, -1 for none)
+ * never publishes its "read done" flag. Tiles that depend on it give up after their
+ * bounded wait, skip their writes and set NX_DEV_TIMEOUT; nothing hangs and the CUDA
+ * context stays usable. The cache is left partially compacted.
+ */
+nx_status nexus_debug_compact(nx_cache* cache, const int32_t* keep_idx, const nx_params* params,
+                              void* ws, size_t ws_bytes, int32_t* dev_status, nx_stream_t stream,
+                              long long skip_signal_tile);
+
+/* Static, human-readable name of a status code. */
+const char* nx_status_string(nx_status status);
+
+/* Kernels launched by the most recent call made from this host thread. */
+int32_t nexus_last_launch_count(void);
+
+/* Name of kernel launch i (0-based) of that call; "" when out of range. Static storage. */
+const char* nexus_last_launch_name(int32_t i);
+
+/*
+ * Benchmark hook: the next entry-point call made from this host thread records
+ * events[i] (cudaEvent_t handles, caller-owned) on its stream right after its i-th
+ * kernel launch, for i < n. The request is consumed by that call; events must stay
+ * valid until it returns.
+ */
+void nexus_profile_next_call(void* const* events, int32_t n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NEXUS_H_ */

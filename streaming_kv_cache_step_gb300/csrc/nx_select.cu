@@ -1,0 +1,171 @@
+// nx_select.cu -- retention set of every slice (Nexus Sampling paper, §2.3).
+//
+// Every slot j carries a 32-bit order key: 0xFFFFFFFF for the forced sink and recency
+// slots, else the monotone image of kappa_j = ln(u_j)/w_j (reservoir) or w_j (top-K).
+// Keeping the B largest composite keys (key, slot) keeps the forced slots plus the K
+// largest kappa, ties to the newer slot. One thread block per slice finds the B-th
+// largest composite by an MSB-first radix select (four 8-bit digit passes on the key,
+// four more on the slot only when the threshold key is tied), then writes the kept
+// slots in ascending order with a block-wide ballot scan.
+#include "nx_internal.cuh"
+
+namespace nx {
+namespace {
+
+constexpr int kSelThreads = 1024;
+
+__global__ void keys_from_w_kernel(nx_cache c, nx_params p, const float* __restrict__ w,
+                                   uint32_t* __restrict__ keys, const int32_t* __restrict__ newlen) {
+  const int slice = blockIdx.x;
+  if (newlen[slice] < 0) return;
+  const int T = c.lens[slice];
+  const int j = blockIdx.y * blockDim.x + threadIdx.x;
+  if (j >= T) return;
+  int l, s, h;
+  slice_coords(c, slice, l, s, h);
+  const long long o = (long long)slice * c.capacity + j;
+  uint32_t key = kForcedKey;
+  if (!(j < p.n_sink || j >= T - p.n_recent)) {
+    const uint32_t head_id = (uint32_t)((p.layer_id_base + l) * c.kv_heads + h);
+    key = candidate_key(w[o], c.pos[row_of(c, l, s, h, j)], p, head_id,
+                        (uint32_t)(p.seq_id_base + s));
+  }
+  keys[o] = key;
+}
+
+// Find digit d with above(d) < need <= above(d) + hist[d], where above(d) counts
+// elements whose digit is larger than d. Run by warp 0; writes (d, above(d), hist[d]).
+__device__ __forceinline__ void pick_digit(const unsigned* hist, int need, int* out3) {
+  const int lane = threadIdx.x & 31;
+  unsigned cnt[8];
+  unsigned mine = 0;
+#pragma unroll
+  for (int b = 0; b < 8; ++b) {
+    cnt[b] = hist[lane * 8 + b];
+    mine += cnt[b];
+  }
+  // above_lane = sum over lanes > lane (bins above this lane's 8 bins)
+  unsigned incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned y = __shfl_down_sync(0xffffffffu, incl, o);
+    if (lane + o < 32) incl += y;
+  }
+  unsigned above = incl - mine;
+#pragma unroll
+  for (int b = 7; b >= 0; --b) {
+    if ((int)above < need && need <= (int)(above + cnt[b])) {
+      out3[0] = lane * 8 + b;
+      out3[1] = (int)above;
+      out3[2] = (int)cnt[b];
+    }
+    above += cnt[b];
+  }
+}
+
+__global__ void __launch_bounds__(kSelThreads)
+select_kernel(nx_cache c, const uint32_t* __restrict__ keys, int32_t* __restrict__ keep,
+              const int32_t* __restrict__ newlen) {
+  const int slice = blockIdx.x;
+  const int nl = newlen[slice];
+  if (nl < 0) return;
+  const int T = c.lens[slice];
+  int32_t* out = keep + (long long)slice * c.capacity;
+  if (T <= nl) {
+    for (int j = threadIdx.x; j < T; j += blockDim.x) out[j] = j;
+    return;
+  }
+  const int B = nl;
+  const uint32_t* kk = keys + (long long)slice * c.capacity;
+  __shared__ unsigned hist[256];
+  __shared__ int pick[3];
+  __shared__ int wcount[kSelThreads / 32];
+
+  // ---- radix select on the key ----
+  uint32_t prefix = 0, pmask = 0;
+  int need = B;
+  int eq_count = 0;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    for (int j = threadIdx.x; j < T; j += blockDim.x) {
+      const uint32_t k = kk[j];
+      if ((k & pmask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) pick_digit(hist, need, pick);
+    __syncthreads();
+    need -= pick[1];
+    eq_count = pick[2];
+    prefix |= (uint32_t)pick[0] << shift;
+    pmask |= 0xFFu << shift;
+    __syncthreads();
+  }
+  const uint32_t tau = prefix;   // the B-th largest key; keep `need` of its eq_count copies
+  // ---- ties at tau: keep the `need` largest slots among key == tau ----
+  int slot_tau = 0;
+  if (eq_count > need) {
+    uint32_t sp = 0, sm = 0;
+    int sneed = need;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+      __syncthreads();
+      for (int j = threadIdx.x; j < T; j += blockDim.x)
+        if (kk[j] == tau && ((uint32_t)j & sm) == sp) atomicAdd(&hist[((uint32_t)j >> shift) & 255u], 1u);
+      __syncthreads();
+      if (threadIdx.x < 32) pick_digit(hist, sneed, pick);
+      __syncthreads();
+      sneed -= pick[1];
+      sp |= (uint32_t)pick[0] << shift;
+      sm |= 0xFFu << shift;
+      __syncthreads();
+    }
+    slot_tau = (int)sp;
+  }
+  // ---- write kept slots, ascending ----
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int base = 0;
+  for (int j0 = 0; j0 < T; j0 += blockDim.x) {
+    const int j = j0 + threadIdx.x;
+    bool take = false;
+    if (j < T) {
+      const uint32_t k = kk[j];
+      take = (k > tau) || (k == tau && j >= slot_tau);
+    }
+    const unsigned bal = __ballot_sync(0xffffffffu, take);
+    if (lane == 0) wcount[warp] = __popc(bal);
+    __syncthreads();
+    int off = base;
+    int tot = 0;
+    for (int w = 0; w < nw; ++w) {
+      const int cw = wcount[w];
+      if (w < warp) off += cw;
+      tot += cw;
+    }
+    if (take) out[off + __popc(bal & ((1u << lane) - 1u))] = j;
+    base += tot;
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_keys_from_w(const nx_cache& c, const nx_params& p, const float* w,
+                               uint32_t* keys, const int32_t* newlen, cudaStream_t st,
+                               int* launches) {
+  const long long slices = (long long)c.layers * c.seqs * c.kv_heads;
+  dim3 grid((unsigned)slices, (c.capacity + 255) / 256);
+  keys_from_w_kernel<<<grid, 256, 0, st>>>(c, p, w, keys, newlen);
+  note_launch(st, launches, "keys_from_w");
+  return cudaGetLastError();
+}
+
+cudaError_t launch_select(const nx_cache& c, const uint32_t* keys, int32_t* keep,
+                          const int32_t* newlen, cudaStream_t st, int* launches) {
+  const long long slices = (long long)c.layers * c.seqs * c.kv_heads;
+  select_kernel<<<(unsigned)slices, kSelThreads, 0, st>>>(c, keys, keep, newlen);
+  note_launch(st, launches, "select");
+  return cudaGetLastError();
+}
+
+}  // namespace nx

@@ -1,0 +1,219 @@
+"""GPU parity: the library's kernels, called through the C ABI, against the CPU oracle on
+the same seeded inputs, at sizes the oracle finishes in seconds (several tiles, ragged
+tails, paged and contiguous layouts, every dtype and window shape)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from harness import (DEV, GpuRun, compare_survivors, oracle_kappa, oracle_slice, score_tol)
+from streaming_kv_cache_step_gb300 import nexus
+from streaming_kv_cache_step_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _cases():
+    paged_lens = np.array([1500, 900, 2048, 100], np.int32)
+    return {
+        "tiny_f32": W.tiny(),
+        "gqa_ragged": W.shrink(W.llama3_8b_layer(), seqs=3, kv_heads=2,
+                               lens=np.array([1000, 37, 700], np.int32), capacity=1024,
+                               budget=np.array([300, 300, 128], np.int32), n_hubs=16),
+        "paged": W.shrink(W.streaming_paged(4), lens=paged_lens, capacity=2048,
+                          budget=np.maximum(64, paged_lens * 2 // 10).astype(np.int32)),
+        "long_w64_h5": W.shrink(W.long_context(), seqs=1, kv_heads=2,
+                                lens=np.array([1500], np.int32), capacity=1536,
+                                budget=np.array([300], np.int32), n_hubs=8, n_bridges=8),
+        "mixture": W.shrink(W.batch16_32layers(), layers=2, seqs=2, kv_heads=2,
+                            lens=np.full(2, 777, np.int32), capacity=800,
+                            budget=np.full(2, 160, np.int32)),
+    }
+
+
+CASES = _cases()
+
+
+def _decode(c, q, wl):
+    k = c["k"][0, 0, 0, : int(c["lens"].reshape(-1)[0])]
+    if k.dtype == np.uint16:
+        k = (k.astype(np.uint32) << 16).view(np.float32)
+        qf = (q.astype(np.uint32) << 16).view(np.float32)
+    else:
+        qf = q
+    qbar = qf.reshape(wl.group, wl.window, wl.head_dim).astype(np.float64).mean(0)
+    return k.astype(np.float64), qbar
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_scores_and_walk_match_oracle(name):
+    wl = CASES[name]
+    run = GpuRun(wl)
+    S, cap, Wn = run.cache.n_slices, wl.capacity, wl.window
+    a = torch.full((S, cap), -1.0, device=DEV)
+    stats = torch.zeros((S, Wn, 2), device=DEV)
+    w = torch.full((S, cap), -1.0, device=DEV)
+    ct = torch.full((S, cap), -1.0, device=DEV)
+    nexus.direct_scores(run.cache, run.q, run.params, a, stats, run.ws, run.status)
+    nexus.walk(run.cache, run.q, run.params, w, ct, run.ws, run.status)
+    run.check_status()
+    a, stats, w, ct = a.cpu().numpy(), stats.cpu().numpy(), w.cpu().numpy(), ct.cpu().numpy()
+    lens = run.lens()
+    for sid in range(S):
+        T = int(lens[sid])
+        c, q, over, ref = oracle_slice(wl, sid)
+        K, Qb = _decode(c, q, wl)
+        o = oracle.slice_scores(K, Qb, wl.walk_len, wl.lam, wl.eps_tie)
+        assert np.all(np.abs(a[sid, :T] - ref["a"][0, :T]) <= score_tol(ref["a"][0, :T], T))
+        assert np.all(np.abs(w[sid, :T] - ref["w"][0, :T]) <= score_tol(ref["w"][0, :T], T))
+        assert np.all(np.abs(ct[sid, :T] - o["ctilde"]) <= score_tol(o["ctilde"], T))
+        assert np.allclose(stats[sid, :, 0], o["rowmax"], rtol=1e-5, atol=1e-4)
+        assert np.allclose(stats[sid, :, 1], o["rowsum"], rtol=1e-4)
+        assert abs(a[sid, :T].astype(np.float64).sum() - 1) < 1e-4
+        assert (a[sid, T:] == -1).all() and (w[sid, T:] == -1).all()   # tail untouched
+
+
+@pytest.mark.parametrize("mode", [nexus.MODE_RESERVOIR, nexus.MODE_TOPK])
+@pytest.mark.parametrize("name", list(CASES))
+def test_select_bitexact_on_oracle_weights(name, mode):
+    wl = CASES[name]
+    run = GpuRun(wl, mode=mode)
+    S, cap = run.cache.n_slices, wl.capacity
+    w_in = torch.zeros((S, cap), device=DEV)
+    refs = []
+    for sid in range(S):
+        _, _, _, ref = oracle_slice(wl, sid, mode=mode)
+        refs.append(ref)
+        T = int(ref["w"].shape[1])       # the oracle's one-slice cache has capacity T
+        w_in[sid, :T] = torch.as_tensor(ref["w"][0], device=DEV)
+    nexus.reservoir_select(w_in, run.cache, run.params, run.keep, run.ws, run.status)
+    run.check_status()
+    keep = run.keep.cpu().numpy()
+    for sid, ref in enumerate(refs):
+        nl = int(ref["newlen"][0])
+        assert np.array_equal(keep[sid, :nl], ref["keep"][0, :nl]), sid
+        assert (keep[sid, nl:] == -1).all()
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_compact_bitexact_on_oracle_keep(name):
+    wl = CASES[name]
+    run = GpuRun(wl)
+    S, cap = run.cache.n_slices, wl.capacity
+    keep_in = torch.full((S, cap), -1, dtype=torch.int32, device=DEV)
+    cs = []
+    for sid in range(S):
+        c, _, _, ref = oracle_slice(wl, sid)
+        nl = int(ref["newlen"][0])
+        keep_in[sid, :nl] = torch.as_tensor(ref["keep"][0, :nl], device=DEV)
+        oracle.compact_slice(c, 0, ref["keep"][0, :nl])
+        cs.append((c, nl))
+    k_before = run.d["k"].clone()
+    nexus.compact(run.cache, keep_in, run.params, run.ws, run.status)
+    run.check_status()
+    lens = run.lens()
+    for sid, (c, nl) in enumerate(cs):
+        assert lens[sid] == nl
+        for name_ in ("k", "v", "pos"):
+            got = W.storage_to_numpy(run.slice_rows(name_, sid, nl))
+            assert np.array_equal(got, c[name_][0, 0, 0, :nl]), (sid, name_)
+    if not wl.page_size:   # rows at or beyond the new length are untouched
+        for sid, (c, nl) in enumerate(cs):
+            layer, s, h = wl.slice_coords(sid)
+            assert torch.equal(run.d["k"][layer, s, h, nl:], k_before[layer, s, h, nl:])
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_evict_step_end_to_end(name):
+    wl = CASES[name]
+    run = GpuRun(wl)
+    S = run.cache.n_slices
+    lens0 = run.lens()
+    nexus.evict_step(run.cache, run.q, run.params, run.keep, run.ws, run.status)
+    run.check_status()
+    keep = run.keep.cpu().numpy()
+    lens = run.lens()
+    for sid in range(S):
+        c, _, _, ref = oracle_slice(wl, sid)
+        nl = int(ref["newlen"][0])
+        T = int(lens0[sid])
+        assert lens[sid] == nl
+        kappa = oracle_kappa(wl, sid, ref["w"][0, :T], c["pos"][0, 0, 0, :T])
+        compare_survivors(keep[sid, :nl], ref["keep"][0, :nl], kappa)
+        # the compacted rows are exactly the original rows at the kept slots
+        for name_ in ("k", "v", "pos"):
+            got = W.storage_to_numpy(run.slice_rows(name_, sid, nl))
+            assert np.array_equal(got, c[name_][0, 0, 0][keep[sid, :nl]]), (sid, name_)
+
+
+def test_zero_walk_gives_direct_scores_and_budget_edges():
+    # H = 0 reproduces the direct score; B = n_sink + n_recent keeps the forced slots only;
+    # T <= B is an identity; T = 1 and T = 0 slices are handled.
+    wl = W.shrink(W.llama3_8b_layer(), seqs=4, kv_heads=1, walk_len=0,
+                  lens=np.array([600, 1, 0, 64], np.int32), capacity=640,
+                  budget=np.array([64, 64, 64, 64], np.int32), n_hubs=4)
+    run = GpuRun(wl)
+    S, cap = run.cache.n_slices, wl.capacity
+    a = torch.zeros((S, cap), device=DEV)
+    w = torch.zeros((S, cap), device=DEV)
+    nexus.direct_scores(run.cache, run.q, run.params, a, None, run.ws, run.status)
+    nexus.walk(run.cache, run.q, run.params, w, None, run.ws, run.status)
+    run.check_status()
+    T = 600
+    ramp = (np.arange(T) / (T - 1)).astype(np.float32) * np.float32(wl.eps_tie)
+    assert np.allclose(w[0, :T].cpu().numpy(), a[0, :T].cpu().numpy() + ramp, rtol=1e-6,
+                       atol=1e-9)
+    assert a[1, 0].item() == pytest.approx(1.0, abs=1e-6)
+    nexus.evict_step(run.cache, run.q, run.params, run.keep, run.ws, run.status)
+    run.check_status()
+    keep = run.keep.cpu().numpy()
+    assert np.array_equal(keep[0, :64], np.r_[np.arange(32), np.arange(600 - 32, 600)])
+    assert keep[1, 0] == 0 and np.array_equal(keep[3, :64], np.arange(64))
+    assert list(run.lens()) == [64, 1, 0, 64]
+
+
+def test_device_argument_faults_are_flagged_not_fatal():
+    wl = W.shrink(W.llama3_8b_layer(), seqs=2, kv_heads=1, lens=np.array([500, 500], np.int32),
+                  capacity=512, budget=np.array([100, 40], np.int32), n_hubs=4)
+    run = GpuRun(wl)
+    before = run.d["k"].clone()
+    nexus.evict_step(run.cache, run.q, run.params, run.keep, run.ws, run.status)
+    torch.cuda.synchronize()
+    assert int(run.status.item()) & nexus.NX_DEV_BAD_BUDGET       # 40 < 32 + 32
+    assert run.lens()[1] == 500                                    # that slice untouched
+    assert torch.equal(run.d["k"][0, 1, 0], before[0, 1, 0])
+    assert run.lens()[0] == 100                                    # the other one evicted
+    run.zero_status()
+    run.d["lens"].view(-1)[1] = 9999                               # > capacity
+    nexus.evict_step(run.cache, run.q, run.params, run.keep, run.ws, run.status)
+    torch.cuda.synchronize()
+    assert int(run.status.item()) & nexus.NX_DEV_BAD_LEN
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    # A compaction tile that never publishes "read done" (test hook) makes the later tiles
+    # that depend on it give up after the bounded wait: NX_DEV_TIMEOUT, no hang, and the
+    # next clean call on the same context succeeds.
+    wl = W.shrink(W.llama3_8b_layer(), seqs=1, kv_heads=1, lens=np.array([8192], np.int32),
+                  capacity=8192, budget=np.array([1638], np.int32), n_hubs=8)
+    run = GpuRun(wl)
+    _, _, _, ref = oracle_slice(wl, 0)
+    keep_in = torch.full((1, wl.capacity), -1, dtype=torch.int32, device=DEV)
+    keep_in[0, :1638] = torch.as_tensor(ref["keep"][0, :1638], device=DEV)
+    lib = nexus.load()
+    import ctypes
+    rc = lib.nexus_debug_compact(ctypes.byref(run.cache.c_struct()),
+                                 ctypes.c_void_p(keep_in.data_ptr()),
+                                 ctypes.byref(run.params.c_struct()),
+                                 ctypes.c_void_p(run.ws.data_ptr()), ctypes.c_size_t(run.ws.numel()),
+                                 ctypes.c_void_p(run.status.data_ptr()),
+                                 ctypes.c_void_p(torch.cuda.current_stream().cuda_stream),
+                                 ctypes.c_longlong(1))
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert int(run.status.item()) & nexus.NX_DEV_TIMEOUT
+    # the context is still usable: a fresh, clean step succeeds
+    run2 = GpuRun(wl)
+    nexus.evict_step(run2.cache, run2.q, run2.params, run2.keep, run2.ws, run2.status)
+    run2.check_status()
+    assert run2.lens()[0] == 1638
