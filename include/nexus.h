@@ -176,6 +176,28 @@ nx_status kv_compact(nx_cache* cache, const int32_t* keep_idx, const nx_params* 
                      void* ws, size_t ws_bytes, int32_t* dev_status, nx_stream_t stream);
 
 /*
+ * kv_compact without a workspace, for callers that cannot allocate device memory:
+ * code that runs where the CUDA allocator must not be called, such as inference
+ * runtimes that plan and own every device byte up front, or real-time paths that may
+ * not pay for (or fail on) an allocation in the middle of a step. The paper has no
+ * counterpart; it is the same compaction as kv_compact, with the same arguments minus
+ * the workspace, and the same results.
+ *
+ * Its scratch (a tile counter, the new lengths, one flag per tile of kCompactRows = 32
+ * rows) lives in a 4 MiB static device array inside libnexus.so, held by every GPU
+ * that loads the library until the process exits. Limit: 256 + 4 * slices (rounded
+ * up to 256) + 4 * slices * ceil(budget_max / 32) (rounded up to 256) bytes must fit
+ * in 4 MiB; larger calls return NX_ERR_WORKSPACE without launching anything. The
+ * function calls no cudaMalloc, cudaFree or other allocating routine.
+ * The first call on each device looks up the array's device address (with that
+ * device current) and must come before any stream capture that includes it. All calls
+ * share the one array: calls that overlap on the GPU (other streams, other host
+ * threads) race and must be serialised by the caller.
+ */
+nx_status kv_compact_noalloc(nx_cache* cache, const int32_t* keep_idx, const nx_params* params,
+                             int32_t* dev_status, nx_stream_t stream);
+
+/*
  * One whole eviction step: scores, walk, reservoir selection and compaction for every
  * slice, with the same results as the four calls above in sequence.
  * keep_idx_out (nullable): int32 [slices][capacity] receives the kept slots.

@@ -1,0 +1,83 @@
+// nx_noalloc.cu -- kv_compact_noalloc: the in-place compaction for callers that cannot
+// allocate device memory themselves (no workspace argument).
+//
+// The compaction's scratch (a tile-claim counter, the new length of every slice and one
+// "read done" flag per tile) lives in the file-scope array below, which every GPU that
+// loads the library holds until the process exits. Host code cannot pass the array's
+// name to a kernel (on the host it is only a stand-in for the device symbol), so the
+// first call on each device looks up the array's device address with
+// cudaGetSymbolAddress while that device is current, and later calls reuse it.
+#include <mutex>
+
+#include "nx_internal.cuh"
+
+namespace nx {
+namespace {
+
+constexpr size_t kNoallocScratchBytes = size_t(4) << 20;   // 4 MiB per device
+constexpr int kNoallocMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kNoallocMaxDevices];
+
+cudaError_t noalloc_scratch_of_current_device(void** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kNoallocMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return cudaSuccess;
+}
+
+constexpr size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+}  // namespace
+}  // namespace nx
+
+extern "C" nx_status kv_compact_noalloc(nx_cache* cache, const int32_t* keep_idx,
+                                        const nx_params* params, int32_t* dev_status,
+                                        nx_stream_t stream) {
+  using namespace nx;
+  // Same argument checks as the workspace-taking entry points (0 = rejected).
+  if (nexus_workspace_bytes(cache, params) == 0) {
+    if (params && cache && params->n_avg > 1) return NX_ERR_UNSUPPORTED;
+    return NX_ERR_INVALID_ARG;
+  }
+  if (!keep_idx || !dev_status) return NX_ERR_INVALID_ARG;
+
+  // Scratch layout inside the static array: claim counter | new lengths | tile flags.
+  WsLayout L{};
+  L.slices = (long long)cache->layers * cache->seqs * cache->kv_heads;
+  L.tiles_per_slice = (params->budget_max + kCompactRows - 1) / kCompactRows;
+  if (L.tiles_per_slice < 1) L.tiles_per_slice = 1;
+  L.work = 0;
+  L.newlen = 256;
+  L.tile_flags = L.newlen + round256((size_t)L.slices * 4);
+  const size_t need = L.tile_flags + round256((size_t)L.slices * L.tiles_per_slice * 4);
+  if (need > kNoallocScratchBytes) return NX_ERR_WORKSPACE;   // sizes beyond the 4 MiB limit
+
+  void* scratch = nullptr;
+  if (noalloc_scratch_of_current_device(&scratch) != cudaSuccess) return NX_ERR_CUDA;
+  char* ws = static_cast<char*>(scratch);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int launches = 0;
+  // The array keeps the previous call's contents: the counter, lengths and flags must
+  // start at zero.
+  if (cudaMemsetAsync(ws, 0, need, st) != cudaSuccess) return NX_ERR_CUDA;
+  int32_t* newlen = reinterpret_cast<int32_t*>(ws + L.newlen);
+  if (launch_newlen(*cache, *params, newlen, dev_status, st, &launches) != cudaSuccess)
+    return NX_ERR_CUDA;
+  if (launch_compact(*cache, *params, L, ws, keep_idx, newlen, dev_status, st, &launches) !=
+      cudaSuccess)
+    return NX_ERR_CUDA;
+  return NX_OK;
+}
