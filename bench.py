@@ -235,6 +235,9 @@ def run_native(args, rank, world, local):
     torch.cuda.synchronize()
     for i in range(K):
         restore()
+        # keep the device busy while the host issues the step, so the events time the
+        # kernels and not the host's launch latency
+        torch.cuda._sleep(200_000)
         starts[i].record(stream)
         step(kev[i])
         ends[i].record(stream)

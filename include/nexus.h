@@ -217,6 +217,12 @@ nx_status nexus_debug_compact(nx_cache* cache, const int32_t* keep_idx, const nx
                               void* ws, size_t ws_bytes, int32_t* dev_status, nx_stream_t stream,
                               long long skip_signal_tile);
 
+/*
+ * Testing hook: with on != 0, the scoring entry points use the CUDA-core scorer even
+ * for shapes the tensor-core scorer covers (process-wide; 0 restores the default).
+ */
+void nexus_debug_force_simt(int32_t on);
+
 /* Static, human-readable name of a status code. */
 const char* nx_status_string(nx_status status);
 

@@ -9,6 +9,7 @@ namespace nx {
 namespace {
 
 thread_local int32_t g_last_launches = 0;
+bool g_force_simt = false;    // set by nexus_debug_force_simt (tests, comparisons)
 constexpr int kMaxLaunchNames = 16;
 thread_local const char* g_launch_names[kMaxLaunchNames];
 thread_local void* const* g_prof_events = nullptr;   // armed by nexus_profile_next_call
@@ -59,7 +60,7 @@ nx_status check_params(const nx_cache* c, const nx_params* p) {
 WsLayout layout_of(const nx_cache* c, const nx_params* p) {
   WsLayout L{};
   L.slices = (long long)c->layers * c->seqs * c->kv_heads;
-  L.max_chunks = (c->capacity + kSimtRows - 1) / kSimtRows;
+  L.max_chunks = (c->capacity + 127) / 128;
   L.stats_stride = (int)align_up(2 * p->window + kMaxPairs, 4);
   L.tiles_per_slice = (p->budget_max + kCompactRows - 1) / kCompactRows;
   if (L.tiles_per_slice < 1) L.tiles_per_slice = 1;
@@ -68,15 +69,22 @@ WsLayout layout_of(const nx_cache* c, const nx_params* p) {
   L.work = o;
   o += 64;
   L.barriers = o;
-  o += align_up((size_t)L.slices * 4, 256);
+  o += align_up((size_t)L.slices * 8, 256);
   L.tile_flags = o;
   o += align_up((size_t)L.slices * L.tiles_per_slice * 4, 256);
+  L.groups_per_slice = (L.max_chunks + 15) / 16;
+  L.group_arrive = o;
+  o += align_up((size_t)L.slices * L.groups_per_slice * 4, 256);
   L.counters_bytes = o - L.counters;
   const size_t cells = (size_t)L.slices * c->capacity;
   L.keys = o;
   o += align_up(cells * 4, 256);
   L.stats = o;
   o += align_up((size_t)L.slices * L.max_chunks * L.stats_stride * 4, 256);
+  L.group_rec = o;
+  o += align_up((size_t)L.slices * L.groups_per_slice * L.stats_stride * 4, 256);
+  L.fin = o;
+  o += align_up((size_t)L.slices * (3 * p->window + kMaxWalk) * 4, 256);
   L.qbar = o;
   o += align_up((size_t)L.slices * p->window * c->head_dim * 4, 256);
   L.newlen = o;
@@ -114,12 +122,22 @@ nx_status finish(cudaError_t e, int launches) {
     if (e_ != cudaSuccess) return finish(e_, launches); \
   } while (0)
 
-// Scores (and whatever `out` asks for) for every slice.
+// Scores (and whatever `out` asks for) for every slice: the tensor-core scorer for the
+// shapes it covers, the CUDA-core scorer otherwise. The counters region must be zero.
 cudaError_t run_scores(const nx_cache& c, const void* q, const nx_params& p, const WsLayout& L,
                        char* ws, const ScoreOut& out, int32_t* dev_status, cudaStream_t st,
                        int* launches) {
-  cudaError_t e = launch_prep(c, q, p, L, ws, dev_status, st, launches);
+  const bool tc = tc_supported(c, p) && !g_force_simt;
+  cudaError_t e = launch_prep(c, q, p, L, ws, dev_status, st, launches, tc ? 2 : 1);
   if (e != cudaSuccess) return e;
+  if (tc) {
+    bool used = false;
+    e = launch_score_tc(c, p, q, L, ws, out, dev_status, st, launches, &used);
+    if (e != cudaSuccess || used) return e;
+    // not launchable for this size: the CUDA-core path needs the fp32 queries
+    e = launch_prep(c, q, p, L, ws, dev_status, st, launches, 1);
+    if (e != cudaSuccess) return e;
+  }
   return launch_score_simt(c, p, L, ws, out, dev_status, st, launches);
 }
 
@@ -160,6 +178,7 @@ nx_status nexus_direct_scores(const nx_cache* cache, const void* q, const nx_par
   if (!q || ((uintptr_t)q & 15u) || !a_out) return NX_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   char* w = static_cast<char*>(ws);
+  NX_TRY(cudaMemsetAsync(w + L.counters, 0, L.counters_bytes, st));
   ScoreOut out{};
   out.a = a_out;
   out.row_stats = row_stats_out;
@@ -179,6 +198,7 @@ nx_status nexus_walk(const nx_cache* cache, const void* q, const nx_params* para
   if (!q || ((uintptr_t)q & 15u) || !w_out) return NX_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   char* w = static_cast<char*>(ws);
+  NX_TRY(cudaMemsetAsync(w + L.counters, 0, L.counters_bytes, st));
   ScoreOut out{};
   out.w = w_out;
   out.ctilde = ctilde_out;
@@ -280,6 +300,8 @@ const char* nx_status_string(nx_status status) {
 }
 
 int32_t nexus_last_launch_count(void) { return g_last_launches; }
+
+void nexus_debug_force_simt(int32_t on) { g_force_simt = on != 0; }
 
 const char* nexus_last_launch_name(int32_t i) {
   return (i >= 0 && i < g_last_launches && i < kMaxLaunchNames) ? g_launch_names[i] : "";

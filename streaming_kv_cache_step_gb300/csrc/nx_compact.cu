@@ -4,10 +4,10 @@
 // keep is ascending with keep[i] >= i, so writing row i can only destroy a source that a
 // destination i' <= i still needs. Destinations are cut into tiles of kCompactRows rows,
 // claimed in increasing order through one global counter. A tile first copies all its
-// sources into shared memory, then publishes "read done", then waits (bounded) for the
-// earlier tiles of its slice whose sources lie in its own destination range, and only
-// then writes. Waits point only to lower tiles, which never wait before publishing, so
-// the scheme cannot deadlock. Rows with keep[i] == i are neither read nor written.
+// sources into shared memory, then publishes "read done", then waits (bounded) until the
+// earlier tiles of its slice have published, and only then writes. Waits point only to
+// lower tiles, which never wait before publishing, so the scheme cannot deadlock. Rows
+// with keep[i] == i are neither read nor written.
 #include "nx_internal.cuh"
 
 namespace nx {
@@ -68,7 +68,7 @@ compact_kernel(nx_cache c, const int32_t* __restrict__ keep, const int32_t* __re
   __shared__ int s_src[kCompactRows];
   __shared__ int s_pos[kCompactRows];
   __shared__ long long s_tile;
-  __shared__ int s_any, s_lo, s_ok;
+  __shared__ int s_any, s_ok;
   uint4* K = reinterpret_cast<uint4*>(c.k);
   uint4* V = reinterpret_cast<uint4*>(c.v);
 
@@ -128,18 +128,12 @@ compact_kernel(nx_cache c, const int32_t* __restrict__ keep, const int32_t* __re
     if (threadIdx.x == 0) {
       __threadfence();
       if (tile != skip_signal_tile) st_release(flag, 1);   // test hook: -1 in normal calls
-      // first destination whose source is at or beyond i0 (keep is ascending)
-      int lo = 0, hi = i0;
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (kp[mid] >= i0) hi = mid; else lo = mid + 1;
-      }
-      s_lo = lo;
       s_ok = 1;
     }
     __syncthreads();
-    // ---- wait for the earlier tiles that read from rows [i0, i0 + n) ----
-    const long long first = (long long)slice * tiles_per_slice + s_lo / kCompactRows;
+    // ---- wait until every earlier tile of the slice has read its sources: only those
+    // can read rows [i0, i0 + n), and none of them waits before publishing ----
+    const long long first = (long long)slice * tiles_per_slice;
     for (long long u = first + threadIdx.x; u < tile; u += blockDim.x)
       if (!wait_at_least(tile_flags + u, 1, dev_status)) s_ok = 0;
     __syncthreads();

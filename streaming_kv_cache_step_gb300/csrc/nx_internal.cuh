@@ -29,15 +29,20 @@ struct WsLayout {
   size_t counters_bytes;
   size_t tile_flags;     // int32 [slices][tiles_per_slice]  (inside counters)
   size_t work;           // int32 [8] global work counters     (inside counters)
-  size_t barriers;       // int32 [slices] slice barriers       (inside counters)
+  size_t barriers;       // int32 [2][slices] slice arrivals, ready flags (inside counters)
   size_t keys;           // uint32 [slices][capacity] order keys
   size_t stats;          // float [slices][max_chunks][stats_stride] partial softmax stats
-  size_t qbar;           // float [slices][W][head_dim] group-mean window queries
+  size_t fin;            // float [slices][3W + kMaxWalk] merged per-slice coefficients
+  size_t group_arrive;   // int32 [slices][groups_per_slice] (inside counters)
+  size_t group_rec;      // float [slices][groups_per_slice][stats_stride]
+  int groups_per_slice;  // chunk records are merged 16 at a time
+  size_t qbar;           // float [slices][W][head_dim] group-mean window queries, or the
+                         // tensor-core scorer's bf16 hi/lo image of the same size
   size_t newlen;         // int32 [slices]
   size_t keep;           // int32 [slices][capacity] kept slots (when the caller gives none)
   size_t total;
   int stats_stride;      // floats per chunk: 2W maxima/sums + kMaxPairs Gram entries (padded)
-  int max_chunks;        // chunks per slice at the CUDA-core tile height
+  int max_chunks;        // chunk records per slice (128-row granularity, covers both scorers)
   int tiles_per_slice;   // compaction tiles per slice (budget_max / kCompactRows, rounded up)
   long long slices;
 };
@@ -194,7 +199,13 @@ struct ScoreOut {
 
 // nx_score.cu
 cudaError_t launch_prep(const nx_cache& c, const void* q, const nx_params& p, const WsLayout& L,
-                        char* ws, int32_t* dev_status, cudaStream_t st, int* launches);
+                        char* ws, int32_t* dev_status, cudaStream_t st, int* launches,
+                        int mode);   // 0: validity only, 1: fp32 Qbar, 2: tensor-core image
+// nx_score_tc.cu: *used is false when the shape is not covered (the caller falls back)
+bool tc_supported(const nx_cache& c, const nx_params& p);
+cudaError_t launch_score_tc(const nx_cache& c, const nx_params& p, const void* q,
+                            const WsLayout& L, char* ws, const ScoreOut& out,
+                            int32_t* dev_status, cudaStream_t st, int* launches, bool* used);
 cudaError_t launch_score_simt(const nx_cache& c, const nx_params& p, const WsLayout& L, char* ws,
                               const ScoreOut& out, int32_t* dev_status, cudaStream_t st,
                               int* launches);

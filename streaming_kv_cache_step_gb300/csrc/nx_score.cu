@@ -27,48 +27,76 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4 raw, float* out) {
   }
 }
 
-// Group-mean window queries and per-slice validity.
+// Per-slice validity and new length (blockIdx.y == 0), plus the group-mean window
+// queries: fp32 rows for the CUDA-core scorer (mode 1), or the tensor-core scorer's
+// shared-memory image (mode 2): bf16(Qbar) and bf16(Qbar - bf16(Qbar)), each as
+// head_dim/64 column blocks of W rows x 128 bytes in the 128-byte swizzled K-major layout
+// (16-byte chunk c of row n stored at chunk c ^ (n mod 8); 8-row groups 1024 bytes apart).
+// Grid: (slices, W); one thread per pair of adjacent features.
 __global__ void prep_kernel(nx_cache c, const void* __restrict__ q, nx_params p,
-                            float* __restrict__ qbar, int32_t* __restrict__ newlen,
-                            int32_t* dev_status) {
+                            void* __restrict__ qout, int32_t* __restrict__ newlen,
+                            int32_t* dev_status, int mode) {
   const int slice = blockIdx.x;
   int l, s, h;
   slice_coords(c, slice, l, s, h);
   const int W = p.window, D = c.head_dim, G = c.group;
-  const int T = c.lens[slice];
-  __shared__ int bad;
-  if (threadIdx.x == 0) {
-    bad = 0;
-    const int B = p.budget[s];
-    if (T < 0 || T > c.capacity) {
-      atomicOr(dev_status, NX_DEV_BAD_LEN);
-      bad = 1;
-    } else if (B < p.n_sink + p.n_recent || B > p.budget_max) {
-      atomicOr(dev_status, NX_DEV_BAD_BUDGET);
-      bad = 1;
-    }
-  }
-  __syncthreads();
-  if (!bad && c.page_size > 0) {
-    const int npg = (T + c.page_size - 1) / c.page_size;
-    for (int i = threadIdx.x; i < npg; i += blockDim.x) {
-      const int pg = c.block_table[(long long)s * c.max_pages_per_seq + i];
-      if (pg < 0 || pg >= c.num_pages || i >= c.max_pages_per_seq) {
-        atomicOr(dev_status, NX_DEV_BAD_PAGE);
+  if (blockIdx.y == 0) {
+    const int T = c.lens[slice];
+    __shared__ int bad;
+    if (threadIdx.x == 0) {
+      bad = 0;
+      const int B = p.budget[s];
+      if (T < 0 || T > c.capacity) {
+        atomicOr(dev_status, NX_DEV_BAD_LEN);
+        bad = 1;
+      } else if (B < p.n_sink + p.n_recent || B > p.budget_max) {
+        atomicOr(dev_status, NX_DEV_BAD_BUDGET);
         bad = 1;
       }
     }
+    __syncthreads();
+    if (!bad && c.page_size > 0) {
+      const int npg = (T + c.page_size - 1) / c.page_size;
+      for (int i = threadIdx.x; i < npg; i += blockDim.x) {
+        const int pg = i < c.max_pages_per_seq
+                           ? c.block_table[(long long)s * c.max_pages_per_seq + i] : -1;
+        if (pg < 0 || pg >= c.num_pages) {
+          atomicOr(dev_status, NX_DEV_BAD_PAGE);
+          bad = 1;
+        }
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) newlen[slice] = bad ? -1 : min(T, p.budget[s]);
   }
-  __syncthreads();
-  if (threadIdx.x == 0) newlen[slice] = bad ? -1 : min(T, p.budget[s]);
+  if (mode == 0) return;
+  const int n = blockIdx.y;                        // window row
+  const int kk = 2 * threadIdx.x;                  // feature pair
+  if (kk >= D) return;
   const long long qbase = (((long long)l * c.seqs + s) * (c.kv_heads * (long long)G) +
-                           (long long)h * G) * W * D;
-  const float invG = 1.0f / (float)G;
-  for (int i = threadIdx.x; i < W * D; i += blockDim.x) {
-    float acc = 0.f;
-    for (int g = 0; g < G; ++g) acc += ld_elem(q, c.dtype, qbase + (long long)g * W * D + i);
-    qbar[(long long)slice * W * D + i] = acc * invG;
+                           (long long)h * G) * W * D + (long long)n * D + kk;
+  float v0 = 0.f, v1 = 0.f;
+  for (int g = 0; g < G; ++g) {
+    v0 += ld_elem(q, c.dtype, qbase + (long long)g * W * D);
+    v1 += ld_elem(q, c.dtype, qbase + (long long)g * W * D + 1);
   }
+  const float invG = 1.0f / (float)G;
+  v0 *= invG;
+  v1 *= invG;
+  if (mode == 1) {
+    float* qb = reinterpret_cast<float*>(qout) + ((long long)slice * W + n) * D + kk;
+    qb[0] = v0;
+    qb[1] = v1;
+    return;
+  }
+  const __nv_bfloat162 hi = __floats2bfloat162_rn(v0, v1);
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(v0 - __low2float(hi), v1 - __high2float(hi));
+  const int KB = D / 64, region = W * 128;
+  const int kb = kk >> 6, byte = (kk & 63) * 2;
+  const int off = (n >> 3) * 1024 + (n & 7) * 128 + ((((byte >> 4) ^ (n & 7)) << 4) | (byte & 15));
+  unsigned char* img = reinterpret_cast<unsigned char*>(qout) + (long long)slice * 2 * KB * region;
+  *reinterpret_cast<__nv_bfloat162*>(img + kb * region + off) = hi;
+  *reinterpret_cast<__nv_bfloat162*>(img + (KB + kb) * region + off) = lo;
 }
 
 template <int N>
@@ -318,10 +346,11 @@ cudaError_t launch_simt_w(const nx_cache& c, const nx_params& p, const WsLayout&
 }  // namespace
 
 cudaError_t launch_prep(const nx_cache& c, const void* q, const nx_params& p, const WsLayout& L,
-                        char* ws, int32_t* dev_status, cudaStream_t st, int* launches) {
-  prep_kernel<<<(unsigned)L.slices, 256, 0, st>>>(
-      c, q, p, reinterpret_cast<float*>(ws + L.qbar), reinterpret_cast<int32_t*>(ws + L.newlen),
-      dev_status);
+                        char* ws, int32_t* dev_status, cudaStream_t st, int* launches,
+                        int mode) {
+  dim3 grid((unsigned)L.slices, mode == 0 ? 1 : p.window);
+  prep_kernel<<<grid, 64, 0, st>>>(c, q, p, ws + L.qbar,
+                                   reinterpret_cast<int32_t*>(ws + L.newlen), dev_status, mode);
   note_launch(st, launches, "prep");
   return cudaGetLastError();
 }

@@ -4,8 +4,8 @@
 // slots, else the monotone image of kappa_j = ln(u_j)/w_j (reservoir) or w_j (top-K).
 // Keeping the B largest composite keys (key, slot) keeps the forced slots plus the K
 // largest kappa, ties to the newer slot. One thread block per slice finds the B-th
-// largest composite by an MSB-first radix select (four 8-bit digit passes on the key,
-// four more on the slot only when the threshold key is tied), then writes the kept
+// largest composite by an MSB-first radix select (three 11/11/10-bit digit passes on the
+// key, three more on the slot only when the threshold key is tied), then writes the kept
 // slots in ascending order with a block-wide ballot scan.
 #include "nx_internal.cuh"
 
@@ -33,15 +33,19 @@ __global__ void keys_from_w_kernel(nx_cache c, nx_params p, const float* __restr
   keys[o] = key;
 }
 
+constexpr int kDigitBits = 11;                  // three passes cover 32 bits
+constexpr int kBins = 1 << kDigitBits;
+constexpr int kBinsPerLane = kBins / 32;
+
 // Find digit d with above(d) < need <= above(d) + hist[d], where above(d) counts
 // elements whose digit is larger than d. Run by warp 0; writes (d, above(d), hist[d]).
 __device__ __forceinline__ void pick_digit(const unsigned* hist, int need, int* out3) {
   const int lane = threadIdx.x & 31;
-  unsigned cnt[8];
+  unsigned cnt[kBinsPerLane];
   unsigned mine = 0;
 #pragma unroll
-  for (int b = 0; b < 8; ++b) {
-    cnt[b] = hist[lane * 8 + b];
+  for (int b = 0; b < kBinsPerLane; ++b) {
+    cnt[b] = hist[lane * kBinsPerLane + b];
     mine += cnt[b];
   }
   // above_lane = sum over lanes > lane (bins above this lane's 8 bins)
@@ -53,9 +57,9 @@ __device__ __forceinline__ void pick_digit(const unsigned* hist, int need, int* 
   }
   unsigned above = incl - mine;
 #pragma unroll
-  for (int b = 7; b >= 0; --b) {
+  for (int b = kBinsPerLane - 1; b >= 0; --b) {
     if ((int)above < need && need <= (int)(above + cnt[b])) {
-      out3[0] = lane * 8 + b;
+      out3[0] = lane * kBinsPerLane + b;
       out3[1] = (int)above;
       out3[2] = (int)cnt[b];
     }
@@ -63,9 +67,34 @@ __device__ __forceinline__ void pick_digit(const unsigned* hist, int need, int* 
   }
 }
 
+// Histogram of kDigitBits-bit digits of the elements matching a prefix, with
+// warp-aggregated shared-memory atomics (one atomic per distinct digit per warp).
+template <bool SMEM>
+__device__ __forceinline__ void digit_hist(const uint32_t* keys, int T, uint32_t pmask,
+                                           uint32_t prefix, int shift, bool by_slot,
+                                           uint32_t tau, unsigned* hist) {
+  const int lane = threadIdx.x & 31;
+  for (int j0 = 0; j0 < T; j0 += blockDim.x) {
+    const int j = j0 + threadIdx.x;
+    uint32_t digit = kBins;
+    if (j < T) {
+      const uint32_t k = keys[j];
+      if (!by_slot) {
+        if ((k & pmask) == prefix) digit = (k >> shift) & (kBins - 1u);
+      } else if (k == tau && ((uint32_t)j & pmask) == prefix) {
+        digit = ((uint32_t)j >> shift) & (kBins - 1u);
+      }
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, digit);
+    if (digit < kBins && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], __popc(peers));
+  }
+}
+
+template <bool SMEM>
 __global__ void __launch_bounds__(kSelThreads)
 select_kernel(nx_cache c, const uint32_t* __restrict__ keys, int32_t* __restrict__ keep,
               const int32_t* __restrict__ newlen) {
+  extern __shared__ uint32_t s_keys[];
   const int slice = blockIdx.x;
   const int nl = newlen[slice];
   if (nl < 0) return;
@@ -76,8 +105,14 @@ select_kernel(nx_cache c, const uint32_t* __restrict__ keys, int32_t* __restrict
     return;
   }
   const int B = nl;
-  const uint32_t* kk = keys + (long long)slice * c.capacity;
-  __shared__ unsigned hist[256];
+  const uint32_t* gk = keys + (long long)slice * c.capacity;
+  const uint32_t* kk = gk;
+  if (SMEM) {
+    for (int j = threadIdx.x; j < T; j += blockDim.x) s_keys[j] = __ldcs(gk + j);
+    kk = s_keys;
+    __syncthreads();
+  }
+  __shared__ unsigned hist[kBins];
   __shared__ int pick[3];
   __shared__ int wcount[kSelThreads / 32];
 
@@ -85,20 +120,20 @@ select_kernel(nx_cache c, const uint32_t* __restrict__ keys, int32_t* __restrict
   uint32_t prefix = 0, pmask = 0;
   int need = B;
   int eq_count = 0;
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+  // digits: bits 21..31, 10..20, 0..9 (the last digit has 10 bits; its upper bin is empty)
+  for (int pass = 0; pass < 3; ++pass) {
+    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+    const uint32_t dmask = pass == 2 ? 0x3FFu : 0x7FFu;
+    for (int i = threadIdx.x; i < kBins; i += blockDim.x) hist[i] = 0;
     __syncthreads();
-    for (int j = threadIdx.x; j < T; j += blockDim.x) {
-      const uint32_t k = kk[j];
-      if ((k & pmask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1u);
-    }
+    digit_hist<SMEM>(kk, T, pmask, prefix, shift, false, 0, hist);
     __syncthreads();
     if (threadIdx.x < 32) pick_digit(hist, need, pick);
     __syncthreads();
     need -= pick[1];
     eq_count = pick[2];
     prefix |= (uint32_t)pick[0] << shift;
-    pmask |= 0xFFu << shift;
+    pmask |= dmask << shift;
     __syncthreads();
   }
   const uint32_t tau = prefix;   // the B-th largest key; keep `need` of its eq_count copies
@@ -107,17 +142,18 @@ select_kernel(nx_cache c, const uint32_t* __restrict__ keys, int32_t* __restrict
   if (eq_count > need) {
     uint32_t sp = 0, sm = 0;
     int sneed = need;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+    for (int pass = 0; pass < 3; ++pass) {
+      const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+      const uint32_t dmask = pass == 2 ? 0x3FFu : 0x7FFu;
+      for (int i = threadIdx.x; i < kBins; i += blockDim.x) hist[i] = 0;
       __syncthreads();
-      for (int j = threadIdx.x; j < T; j += blockDim.x)
-        if (kk[j] == tau && ((uint32_t)j & sm) == sp) atomicAdd(&hist[((uint32_t)j >> shift) & 255u], 1u);
+      digit_hist<SMEM>(kk, T, sm, sp, shift, true, tau, hist);
       __syncthreads();
       if (threadIdx.x < 32) pick_digit(hist, sneed, pick);
       __syncthreads();
       sneed -= pick[1];
       sp |= (uint32_t)pick[0] << shift;
-      sm |= 0xFFu << shift;
+      sm |= dmask << shift;
       __syncthreads();
     }
     slot_tau = (int)sp;
@@ -163,7 +199,24 @@ cudaError_t launch_keys_from_w(const nx_cache& c, const nx_params& p, const floa
 cudaError_t launch_select(const nx_cache& c, const uint32_t* keys, int32_t* keep,
                           const int32_t* newlen, cudaStream_t st, int* launches) {
   const long long slices = (long long)c.layers * c.seqs * c.kv_heads;
-  select_kernel<<<(unsigned)slices, kSelThreads, 0, st>>>(c, keys, keep, newlen);
+  // keys of a slice in shared memory when they fit (up to 48K slots), else from L2
+  constexpr int kSmemKeys = 48 * 1024;
+  if (c.capacity <= kSmemKeys) {
+    const size_t bytes = (size_t)c.capacity * 4;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    static bool attr_set[64] = {};
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+      cudaError_t e = cudaFuncSetAttribute(select_kernel<true>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kSmemKeys * 4);
+      if (e != cudaSuccess) return e;
+      attr_set[dev] = true;
+    }
+    select_kernel<true><<<(unsigned)slices, kSelThreads, bytes, st>>>(c, keys, keep, newlen);
+  } else {
+    select_kernel<false><<<(unsigned)slices, kSelThreads, 0, st>>>(c, keys, keep, newlen);
+  }
   note_launch(st, launches, "select");
   return cudaGetLastError();
 }

@@ -27,7 +27,7 @@ MODE_RESERVOIR, MODE_TOPK = 0, 1
 SYMBOLS = ("nexus_workspace_bytes", "nexus_direct_scores", "nexus_walk",
            "nexus_reservoir_select", "kv_compact", "nexus_evict_step", "nx_status_string",
            "nexus_last_launch_count", "nexus_debug_compact", "nexus_last_launch_name",
-           "nexus_profile_next_call")
+           "nexus_profile_next_call", "nexus_debug_force_simt")
 
 
 class NexusError(RuntimeError):
@@ -86,8 +86,15 @@ def load(path: str = LIB_PATH):
             lib.nexus_last_launch_name.restype = ctypes.c_char_p
             lib.nexus_profile_next_call.argtypes = [ctypes.c_void_p, ctypes.c_int32]
             lib.nexus_profile_next_call.restype = None
+            lib.nexus_debug_force_simt.argtypes = [ctypes.c_int32]
+            lib.nexus_debug_force_simt.restype = None
             _lib = lib
     return _lib
+
+
+def force_simt(on: bool) -> None:
+    """Route scoring to the CUDA-core scorer even where the tensor-core one applies."""
+    load().nexus_debug_force_simt(1 if on else 0)
 
 
 def status_string(status: int) -> str:

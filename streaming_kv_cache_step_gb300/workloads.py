@@ -44,7 +44,7 @@ SQRT3 = float(np.float32(math.sqrt(3.0)))
 DATA_SEED_BASE = 0x5EED0
 PHILOX_SEED = 0x243F6A8885A308D3
 
-TAG_K, TAG_V, TAG_TOPIC = 1, 2, 3
+TAG_K, TAG_V, TAG_TOPIC, TAG_SCALE = 1, 2, 3, 4
 
 
 def _mix32_int(x: int) -> int:
@@ -174,6 +174,10 @@ def plant(wl: Workload, sid: int) -> dict:
     Hubs and bridges sit at distinct positions outside the forced sink and
     recency slots of the first step.
     """
+    return _memo("plant", wl, sid, lambda: _plant(wl, sid))
+
+
+def _plant(wl: Workload, sid: int) -> dict:
     layer, s, h = wl.slice_coords(sid)
     T = int(wl.lens[s])
     lo, hi = wl.n_sink, max(wl.n_sink + 1, T - wl.n_recent)
@@ -195,6 +199,10 @@ def _base_rows(wl: Workload, sid: int, positions: np.ndarray) -> np.ndarray:
 
 def _planted_rows(wl: Workload, sid: int) -> tuple[np.ndarray, np.ndarray]:
     """(positions, binary32 rows) that replace the base keys of one slice."""
+    return _memo("rows", wl, sid, lambda: _planted_rows_uncached(wl, sid))
+
+
+def _planted_rows_uncached(wl: Workload, sid: int) -> tuple[np.ndarray, np.ndarray]:
     pl = plant(wl, sid)
     d = wl.head_dim
     hubs, bridges = pl["hubs"], pl["bridges"]
@@ -234,24 +242,40 @@ def _planted_rows(wl: Workload, sid: int) -> tuple[np.ndarray, np.ndarray]:
 # ---------------------------------------------------------------------------
 
 def _row_scale(wl: Workload, sids: torch.Tensor, pos: torch.Tensor, device) -> torch.Tensor | None:
+    """Log-normal row norms exp(sigma * zeta), zeta ~ Irwin-Hall(4) drawn per (slice,
+    position) from the hash. The sum m of four 16-bit words indexes a 4096-entry binary32
+    table of exp(sigma * zeta(m)) built by numpy, so CPU and GPU get the same bits."""
     if wl.key_kind != "lognormal":
         return None
-    # log-normal row norms: exp(sigma * zeta) with zeta ~ N(0,1) drawn per
-    # (slice, position) by numpy on the host, then copied.
-    sc = np.empty(tuple(pos.shape), np.float32)
-    sid_np = sids.cpu().numpy()
-    pos_np = pos.cpu().numpy()
-    for i, sid in enumerate(sid_np):
-        rng = _rng(wl, 21, int(sid))
-        mx = int(pos_np[i].max()) + 1 if pos_np[i].size else 0
-        zeta = rng.standard_normal(mx)
-        sc[i] = np.exp(wl.lognormal_sigma * zeta[pos_np[i]]).astype(np.float32)
-    return torch.as_tensor(sc, device=device)
+    keys = torch.tensor([stream_key(wl.seed, TAG_SCALE, int(s)) for s in sids.cpu().tolist()],
+                        dtype=torch.int64, device=device)[:, None]
+    h1 = hash_words(keys, 2 * pos)
+    h2 = hash_words(keys, 2 * pos + 1)
+    m = (h1 & 0xFFFF) + (h1 >> 16) + (h2 & 0xFFFF) + (h2 >> 16)        # [0, 4 * 65535]
+    centers = (np.arange(4096, dtype=np.float64) * 64 + 31.5 + 2.0) / 65536.0
+    table = np.exp(wl.lognormal_sigma * (centers - 2.0) * math.sqrt(3.0)).astype(np.float32)
+    return torch.as_tensor(table, device=device)[m >> 6]
+
+
+_CACHE: dict = {}
+
+
+def _memo(kind: str, wl: Workload, sid: int, fn):
+    key = (kind, sid, repr(sorted((k, v) for k, v in vars(wl).items()
+                                  if not isinstance(v, np.ndarray))),
+           wl.lens.tobytes())
+    if key not in _CACHE:
+        if len(_CACHE) > 200000:
+            _CACHE.clear()
+        _CACHE[key] = fn()
+    return _CACHE[key]
 
 
 def _centroids(wl: Workload, layer: int, h: int) -> np.ndarray:
-    rng = _rng(wl, 31, layer, h)
-    return rng.standard_normal((wl.n_topics, wl.head_dim)).astype(np.float32)
+    def make():
+        rng = _rng(wl, 31, layer, h)
+        return rng.standard_normal((wl.n_topics, wl.head_dim)).astype(np.float32)
+    return _memo("mu", wl, layer * 65536 + h, make)
 
 
 def _key_rows(wl: Workload, sids: torch.Tensor, pos: torch.Tensor, device) -> torch.Tensor:
@@ -296,7 +320,10 @@ def key_rows(wl: Workload, sids, pos, device) -> torch.Tensor:
     pos = torch.as_tensor(pos, dtype=torch.int64)
     z = _key_rows(wl, sids, pos, device)
     if wl.n_hubs or wl.n_bridges:
+        pmin = pos.amin(dim=1).tolist() if pos.numel() else []
         for i, sid in enumerate(sids.tolist()):
+            if pmin and pmin[i] >= int(wl.lens[wl.slice_coords(sid)[1]]):
+                continue            # appended tokens are never planted
             where, rows = _planted_rows(wl, sid)
             if where.size == 0:
                 continue
@@ -333,8 +360,10 @@ def query_rows(wl: Workload, sid: int, step: int) -> np.ndarray:
     hubs = pl["hubs"]
     if hubs.size == 0:
         return noise.astype(np.float32)
-    hub_keys = key_rows(wl, [sid], hubs[None, :], "cpu")[0].numpy().astype(np.float64)
-    unit = hub_keys / np.linalg.norm(hub_keys, axis=1, keepdims=True)
+    def make_unit():
+        hk = key_rows(wl, [sid], hubs[None, :], "cpu")[0].numpy().astype(np.float64)
+        return hk / np.linalg.norm(hk, axis=1, keepdims=True)
+    unit = _memo("unit", wl, sid, make_unit)
     if wl.zipf > 0:
         ranks = np.arange(1, hubs.size + 1, dtype=np.float64)
         p = ranks ** (-wl.zipf)
@@ -421,8 +450,10 @@ def make_cache(wl: Workload, device, chunk_rows: int = 1 << 22) -> dict:
     return out
 
 
-def slice_numpy_cache(wl: Workload, sid: int, positions=None, step: int = 0) -> tuple[dict, np.ndarray, dict]:
-    """A one-slice contiguous numpy cache (oracle input) holding `positions` in order.
+def slice_numpy_cache(wl: Workload, sid: int, positions=None, step: int = 0,
+                      capacity: int | None = None) -> tuple[dict, np.ndarray, dict]:
+    """A one-slice contiguous numpy cache (oracle input) holding `positions` in order,
+    with room for `capacity` rows (default: exactly the positions given).
 
     Returns (cache, queries [1][1][G][W][d] storage-dtype numpy, params overrides with
     seq_id_base / layer_id_base so the Philox stream matches the full cache).
@@ -432,7 +463,7 @@ def slice_numpy_cache(wl: Workload, sid: int, positions=None, step: int = 0) -> 
         positions = np.arange(int(wl.lens[s]))
     positions = np.asarray(positions, dtype=np.int64)
     T = positions.size
-    cap = max(T, 1)
+    cap = max(T, 1) if capacity is None else max(capacity, T, 1)
     kr = to_storage(key_rows(wl, [sid], positions[None, :], "cpu")[0], wl.dtype)
     vr = to_storage(value_rows(wl, torch.tensor([sid]), torch.as_tensor(positions)[None, :], "cpu")[0],
                     wl.dtype)
@@ -581,6 +612,47 @@ def append_tokens(wl: Workload, cache: dict, step: int, sids=None, slice_index=N
             vf[row, cur:cur + n] = vr.to(v.dtype)
             pf[row, cur:cur + n] = pr
         lens_flat[row] = cur + n
+
+
+def append_tokens_all(wl: Workload, cache: dict, step: int) -> None:
+    """append_tokens for every slice of a make_cache cache at once (same bits)."""
+    n = wl.append_per_step
+    if n <= 0:
+        return
+    batch = max(1, (1 << 26) // (n * wl.head_dim))     # bound the hash temporaries
+    k, v, pos, lens = cache["k"], cache["v"], cache["pos"], cache["lens"]
+    dev = k.device
+    lens_flat = lens.reshape(-1)
+    ns = wl.n_slices
+    sids = np.arange(ns)
+    s_of = (sids // wl.kv_heads) % wl.seqs
+    l_of = sids // (wl.kv_heads * wl.seqs)
+    h_of = sids % wl.kv_heads
+    p0 = wl.lens[s_of].astype(np.int64) + (step - 1) * n
+    ar = torch.arange(n, device=dev)
+    if int(lens_flat.max()) + n > wl.capacity:
+        raise ValueError("append would exceed the slice capacity")
+    for b0 in range(0, ns, batch):
+        b1 = min(ns, b0 + batch)
+        P = torch.as_tensor(p0[b0:b1, None] + np.arange(n)[None, :])
+        kr = to_storage(key_rows(wl, sids[b0:b1], P, dev), wl.dtype).to(k.dtype)
+        vr = to_storage(value_rows(wl, torch.as_tensor(sids[b0:b1]), P, dev), wl.dtype).to(v.dtype)
+        pr = P.to(device=dev, dtype=torch.int32)
+        slots = lens_flat[b0:b1].long()[:, None] + ar[None, :]
+        li = torch.as_tensor(l_of[b0:b1], device=dev)[:, None].expand(-1, n)
+        hi = torch.as_tensor(h_of[b0:b1], device=dev)[:, None].expand(-1, n)
+        si = torch.as_tensor(s_of[b0:b1], device=dev)[:, None].expand(-1, n)
+        if wl.page_size:
+            ps = wl.page_size
+            pages = cache["block_table"].long()[si, slots // ps]
+            k[li, pages, hi, slots % ps] = kr
+            v[li, pages, hi, slots % ps] = vr
+            pos[li, pages, hi, slots % ps] = pr
+        else:
+            k[li, si, hi, slots] = kr
+            v[li, si, hi, slots] = vr
+            pos[li, si, hi, slots] = pr
+        lens_flat[b0:b1] += n
 
 
 def numpy_cache_as_torch(cache: dict) -> dict:

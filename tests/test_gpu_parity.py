@@ -217,3 +217,31 @@ def test_bounded_wait_times_out_and_context_survives():
     nexus.evict_step(run2.cache, run2.q, run2.params, run2.keep, run2.ws, run2.status)
     run2.check_status()
     assert run2.lens()[0] == 1638
+
+
+@pytest.mark.parametrize("name", ["gqa_ragged", "paged", "long_w64_h5", "mixture"])
+def test_tensor_core_scorer_matches_cuda_core_scorer(name):
+    # the bf16 shapes run on the tcgen05 scorer by default; the CUDA-core scorer is an
+    # independent kernel on the same inputs: both must agree within the score tolerance
+    wl = CASES[name]
+    run = GpuRun(wl)
+    S, cap = run.cache.n_slices, wl.capacity
+    outs = []
+    for simt in (False, True):
+        nexus.force_simt(simt)
+        try:
+            w = torch.full((S, cap), -1.0, device=DEV)
+            ct = torch.full((S, cap), -1.0, device=DEV)
+            nexus.walk(run.cache, run.q, run.params, w, ct, run.ws, run.status)
+            run.check_status()
+            names = nexus.last_launch_names()
+        finally:
+            nexus.force_simt(False)
+        assert ("score_tc" in names) != simt, names
+        outs.append((w.cpu().numpy(), ct.cpu().numpy()))
+    (w_tc, c_tc), (w_si, c_si) = outs
+    lens = run.lens()
+    for sid in range(S):
+        T = int(lens[sid])
+        assert np.all(np.abs(w_tc[sid, :T] - w_si[sid, :T]) <= 2 * score_tol(w_si[sid, :T], T))
+        assert np.all(np.abs(c_tc[sid, :T] - c_si[sid, :T]) <= 2 * score_tol(c_si[sid, :T], T))
