@@ -221,6 +221,7 @@ def run_native(args, rank, world, local):
     assert int(status.item()) == 0, f"device status {int(status.item())}"
     launch_names = nexus.last_launch_names()
     nl = len(launch_names)
+    scorer_cfg = nexus.scorer_config() if "score_tc" in launch_names else None
 
     # ---- timed region ----
     sampler = ClockSampler(local)
@@ -331,6 +332,7 @@ def run_native(args, rank, world, local):
                e2e=dict(value=round(e2e_value, 1), unit=UNIT, h2d_bytes_per_step=h2d,
                         d2h_bytes_per_step=d2h, steps=e2e_steps),
                gpu_launches=launches, kernels_us={k: round(v, 3) for k, v in per_kernel.items()},
+               scorer=scorer_cfg,
                clocks=clocks)
     return out, wl
 

@@ -223,6 +223,20 @@ nx_status nexus_debug_compact(nx_cache* cache, const int32_t* keep_idx, const nx
  */
 void nexus_debug_force_simt(int32_t on);
 
+/*
+ * Diagnostics of the tensor-core scorer (not part of the method):
+ * nexus_debug_set_trace installs a device buffer of grid x 1024 x 2 int64 that later
+ * launches fill with (phase tag, globaltimer ns) pairs per CTA; NULL turns it off.
+ * nexus_debug_scorer_config writes the last launch's configuration from this host
+ * thread: CTAs per SM used, per SM reported by the occupancy API, grid, tiles per chunk,
+ * TMEM buffers, chunks per slice, TMEM columns, dynamic shared memory bytes. When the
+ * last call could not use the tensor-core scorer, the first entry is negative: -1 no
+ * tensor-map encoder, -2 too many rows for one tensor map, -3 tensor map rejected,
+ * -4 a slice has more chunks than co-resident CTAs, -5 the cooperative launch did not fit.
+ */
+void nexus_debug_set_trace(long long* device_buffer);
+void nexus_debug_scorer_config(int32_t* out8);
+
 /* Static, human-readable name of a status code. */
 const char* nx_status_string(nx_status status);
 

@@ -303,6 +303,12 @@ int32_t nexus_last_launch_count(void) { return g_last_launches; }
 
 void nexus_debug_force_simt(int32_t on) { g_force_simt = on != 0; }
 
+void nexus_debug_set_trace(long long* device_buffer) { tc_set_trace(device_buffer); }
+
+void nexus_debug_scorer_config(int32_t* out8) {
+  if (out8) tc_last_config(out8);
+}
+
 const char* nexus_last_launch_name(int32_t i) {
   return (i >= 0 && i < g_last_launches && i < kMaxLaunchNames) ? g_launch_names[i] : "";
 }

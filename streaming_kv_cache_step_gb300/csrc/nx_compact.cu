@@ -5,9 +5,12 @@
 // destination i' <= i still needs. Destinations are cut into tiles of kCompactRows rows,
 // claimed in increasing order through one global counter. A tile first copies all its
 // sources into shared memory, then publishes "read done", then waits (bounded) until the
-// earlier tiles of its slice have published, and only then writes. Waits point only to
-// lower tiles, which never wait before publishing, so the scheme cannot deadlock. Rows
-// with keep[i] == i are neither read nor written.
+// earlier tiles of its slice have published, and only then writes. Each block holds two
+// tiles: the next one's reads (cp.async) overlap the current one's wait and writes.
+// No deadlock: the lowest unpublished tile is either a block's current tile, published
+// without waiting, or its next one, published once the current tile -- which only waits
+// on lower, hence published, tiles -- is written. Rows with keep[i] == i are neither
+// read nor written.
 #include "nx_internal.cuh"
 
 namespace nx {
@@ -56,6 +59,28 @@ __global__ void newlen_kernel(nx_cache c, nx_params p, int32_t* __restrict__ new
   newlen[slice] = slice_ok(c, p, (int)slice, dev_status) ? min(c.lens[slice], p.budget[s]) : -1;
 }
 
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
+               "l"(gsrc)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
+// Per-buffer description of a claimed tile.
+struct TileSlot {
+  long long tile;   // >= total: none
+  int slice, t, i0, n, nl, l, s, h;
+  int moves;        // any row with keep[i] != i
+};
+
+// Two shared-memory buffers: while tile c's rows are written from one, tile c+1's sources
+// stream into the other with cp.async.
 __global__ void __launch_bounds__(kCompactThreads)
 compact_kernel(nx_cache c, const int32_t* __restrict__ keep, const int32_t* __restrict__ newlen,
                int* tile_flags, unsigned long long* work, int tiles_per_slice,
@@ -63,95 +88,105 @@ compact_kernel(nx_cache c, const int32_t* __restrict__ keep, const int32_t* __re
   extern __shared__ __align__(16) unsigned char smem[];
   const int row_bytes = c.head_dim * (c.dtype == NX_DTYPE_BF16 ? 2 : 4);
   const int chunks = row_bytes / 16;                    // 16-byte pieces per row
-  uint4* sk = reinterpret_cast<uint4*>(smem);
-  uint4* sv = sk + kCompactRows * chunks;
-  __shared__ int s_src[kCompactRows];
-  __shared__ int s_pos[kCompactRows];
-  __shared__ long long s_tile;
-  __shared__ int s_any, s_ok;
+  const int per_buf = 2 * kCompactRows * chunks;        // K then V
+  uint4* bufs = reinterpret_cast<uint4*>(smem);
+  __shared__ int s_src[2][kCompactRows];
+  __shared__ int s_pos[2][kCompactRows];
+  __shared__ TileSlot s_slot[2];
+  __shared__ long long s_claim;
+  __shared__ int s_ok;
   uint4* K = reinterpret_cast<uint4*>(c.k);
   uint4* V = reinterpret_cast<uint4*>(c.v);
 
+  // claim the next tile (in increasing order over the whole grid) and start its reads
+  auto stage = [&](int b) {
+    if (threadIdx.x == 0) s_claim = (long long)atomicAdd(work, 1ULL);
+    __syncthreads();
+    TileSlot sl;
+    sl.tile = s_claim;
+    sl.moves = 0;
+    sl.n = 0;
+    if (sl.tile < total_tiles) {
+      sl.slice = (int)(sl.tile / tiles_per_slice);
+      sl.t = (int)(sl.tile % tiles_per_slice);
+      sl.nl = newlen[sl.slice];
+      sl.i0 = sl.t * kCompactRows;
+      slice_coords(c, sl.slice, sl.l, sl.s, sl.h);
+      if (sl.nl >= 0 && sl.i0 < sl.nl) sl.n = min(kCompactRows, sl.nl - sl.i0);
+    }
+    const int32_t* kp = (sl.n > 0) ? keep + (long long)sl.slice * c.capacity : nullptr;
+    if (threadIdx.x < kCompactRows) {
+      const int i = threadIdx.x;
+      const int src = (i < sl.n) ? kp[sl.i0 + i] : 0;
+      s_src[b][i] = src;
+      const bool mv = i < sl.n && src != sl.i0 + i;
+      if (mv) s_pos[b][i] = c.pos[row_of(c, sl.l, sl.s, sl.h, src)];
+      const unsigned any = __ballot_sync(0xffffffffu, mv);
+      if (i == 0) {
+        sl.moves = any != 0;
+        s_slot[b] = sl;
+      }
+    }
+    __syncthreads();
+    sl = s_slot[b];
+    if (sl.moves) {
+      uint4* bk = bufs + b * per_buf;
+      uint4* bv = bk + kCompactRows * chunks;
+      for (int e = threadIdx.x; e < sl.n * chunks; e += blockDim.x) {
+        const int i = e / chunks, ch = e - i * chunks;
+        const int src = s_src[b][i];
+        if (src != sl.i0 + i) {
+          const long long r = row_of(c, sl.l, sl.s, sl.h, src);
+          cp_async16(bk + e, K + r * chunks + ch);
+          cp_async16(bv + e, V + r * chunks + ch);
+        }
+      }
+    }
+    cp_async_commit();
+  };
+
+  int b = 0;
+  stage(b);
   for (;;) {
-    if (threadIdx.x == 0) s_tile = (long long)atomicAdd(work, 1ULL);
-    __syncthreads();
-    const long long tile = s_tile;
-    if (tile >= total_tiles) return;
-    const int slice = (int)(tile / tiles_per_slice);
-    const int t = (int)(tile % tiles_per_slice);
-    const int nl = newlen[slice];
-    int* flag = tile_flags + tile;
-    const int i0 = t * kCompactRows;
-    if (nl < 0 || i0 >= nl) {
-      if (threadIdx.x == 0) {
-        if (t == 0 && nl >= 0) c.lens[slice] = nl;
-        st_release(flag, 1);
-      }
-      __syncthreads();
-      continue;
-    }
-    int l, s, h;
-    slice_coords(c, slice, l, s, h);
-    const int n = min(kCompactRows, nl - i0);
-    const int32_t* kp = keep + (long long)slice * c.capacity;
-    if (threadIdx.x == 0) s_any = 0;
-    __syncthreads();
-    if (threadIdx.x < n) {
-      const int src = kp[i0 + threadIdx.x];
-      s_src[threadIdx.x] = src;
-      if (src != i0 + threadIdx.x) s_any = 1;
-    }
-    __syncthreads();
-    if (!s_any) {            // identity tile: nothing to move
-      if (threadIdx.x == 0) {
-        if (t == 0) c.lens[slice] = nl;
-        st_release(flag, 1);
-      }
-      __syncthreads();
-      continue;
-    }
-    // ---- read every moved source row into shared memory ----
-    for (int e = threadIdx.x; e < n * chunks; e += blockDim.x) {
-      const int i = e / chunks, ch = e % chunks;
-      const int src = s_src[i];
-      if (src != i0 + i) {
-        const long long r = row_of(c, l, s, h, src);
-        sk[e] = K[r * chunks + ch];
-        sv[e] = V[r * chunks + ch];
-      }
-    }
-    if (threadIdx.x < n) {
-      const int src = s_src[threadIdx.x];
-      if (src != i0 + (int)threadIdx.x) s_pos[threadIdx.x] = c.pos[row_of(c, l, s, h, src)];
-    }
+    const TileSlot cur = s_slot[b];
+    if (cur.tile >= total_tiles) break;
+    // the current tile's reads are complete: publish "read done"
+    cp_async_wait_all();
     __syncthreads();
     if (threadIdx.x == 0) {
       __threadfence();
-      if (tile != skip_signal_tile) st_release(flag, 1);   // test hook: -1 in normal calls
+      if (cur.tile != skip_signal_tile) st_release(tile_flags + cur.tile, 1);   // test hook
+      if (cur.t == 0 && cur.tile < total_tiles && cur.nl >= 0) c.lens[cur.slice] = cur.nl;
       s_ok = 1;
     }
-    __syncthreads();
-    // ---- wait until every earlier tile of the slice has read its sources: only those
-    // can read rows [i0, i0 + n), and none of them waits before publishing ----
-    const long long first = (long long)slice * tiles_per_slice;
-    for (long long u = first + threadIdx.x; u < tile; u += blockDim.x)
-      if (!wait_at_least(tile_flags + u, 1, dev_status)) s_ok = 0;
-    __syncthreads();
-    if (s_ok) {
-      for (int e = threadIdx.x; e < n * chunks; e += blockDim.x) {
-        const int i = e / chunks, ch = e % chunks;
-        if (s_src[i] != i0 + i) {
-          const long long r = row_of(c, l, s, h, i0 + i);
-          K[r * chunks + ch] = sk[e];
-          V[r * chunks + ch] = sv[e];
+    // start the next tile's reads; they proceed while this tile waits and writes
+    stage(b ^ 1);
+    if (cur.moves) {
+      // every earlier tile of the slice has read its sources (only those can read rows
+      // [i0, i0 + n); none of them waits before publishing)
+      const long long first = (long long)cur.slice * tiles_per_slice;
+      for (long long u = first + threadIdx.x; u < cur.tile; u += blockDim.x)
+        if (!wait_at_least(tile_flags + u, 1, dev_status)) s_ok = 0;
+      __syncthreads();
+      if (s_ok) {
+        const uint4* bk = bufs + b * per_buf;
+        const uint4* bv = bk + kCompactRows * chunks;
+        for (int e = threadIdx.x; e < cur.n * chunks; e += blockDim.x) {
+          const int i = e / chunks, ch = e - i * chunks;
+          if (s_src[b][i] != cur.i0 + i) {
+            const long long r = row_of(c, cur.l, cur.s, cur.h, cur.i0 + i);
+            K[r * chunks + ch] = bk[e];
+            V[r * chunks + ch] = bv[e];
+          }
         }
+        if (threadIdx.x < cur.n && s_src[b][threadIdx.x] != cur.i0 + (int)threadIdx.x)
+          c.pos[row_of(c, cur.l, cur.s, cur.h, cur.i0 + threadIdx.x)] = s_pos[b][threadIdx.x];
       }
-      if (threadIdx.x < n && s_src[threadIdx.x] != i0 + (int)threadIdx.x)
-        c.pos[row_of(c, l, s, h, i0 + threadIdx.x)] = s_pos[threadIdx.x];
-      if (threadIdx.x == 0 && t == 0) c.lens[slice] = nl;
     }
     __syncthreads();
+    b ^= 1;
   }
+  cp_async_wait_all();
 }
 
 }  // namespace
@@ -169,7 +204,7 @@ cudaError_t launch_compact(const nx_cache& c, const nx_params& p, const WsLayout
                            cudaStream_t st, int* launches, long long skip_signal_tile) {
   (void)p;
   const int row_bytes = c.head_dim * (c.dtype == NX_DTYPE_BF16 ? 2 : 4);
-  const size_t smem = 2 * (size_t)kCompactRows * row_bytes;
+  const size_t smem = 2 * 2 * (size_t)kCompactRows * row_bytes;   // two buffers of K + V
   int dev = 0, sms = 0, per_sm = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

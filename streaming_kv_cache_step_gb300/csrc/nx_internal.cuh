@@ -15,7 +15,7 @@ namespace nx {
 // ---------------------------------------------------------------------------
 constexpr int kMaxWindow = 64;        // W <= 64
 constexpr int kMaxWalk = 8;           // H <= 8
-constexpr int kMaxPairs = kMaxWalk * (kMaxWalk + 1) / 2;
+constexpr int kMaxPairs = kMaxWalk * (kMaxWalk - 1) / 2;   // walk-row pairs u < t
 constexpr int kSimtRows = 256;        // rows per thread block in the CUDA-core scorer
 constexpr int kCompactRows = 32;      // destination rows per compaction tile
 constexpr long long kSpinLimit = 1LL << 22;   // bounded waits: ~0.3-1 s at most
@@ -47,17 +47,16 @@ struct WsLayout {
   long long slices;
 };
 
-// Walk-row pairs (t, u), t <= u < kMaxWalk, in a fixed packed order.
-__host__ __device__ constexpr int pair_index(int t, int u) {
-  return t * kMaxWalk - t * (t - 1) / 2 + (u - t);
-}
-__host__ __device__ inline void pair_of(int k, int& t, int& u) {
-  t = 0;
-  while (k >= kMaxWalk - t) {
-    k -= kMaxWalk - t;
+// Walk-row pairs (u, t), u < t < kMaxWalk, packed in the order of t then u. The walk
+// recurrence gamma_t = 1 + sum_{u<t} gamma_u <P_t, P_u> uses exactly these entries.
+__host__ __device__ constexpr int pair_index(int u, int t) { return t * (t - 1) / 2 + u; }
+__host__ __device__ inline void pair_of(int k, int& u, int& t) {
+  t = 1;
+  while (k >= t) {
+    k -= t;
     ++t;
   }
-  u = t + k;
+  u = k;
 }
 
 // ---------------------------------------------------------------------------
@@ -203,6 +202,8 @@ cudaError_t launch_prep(const nx_cache& c, const void* q, const nx_params& p, co
                         int mode);   // 0: validity only, 1: fp32 Qbar, 2: tensor-core image
 // nx_score_tc.cu: *used is false when the shape is not covered (the caller falls back)
 bool tc_supported(const nx_cache& c, const nx_params& p);
+void tc_set_trace(long long* buf);
+void tc_last_config(int32_t* out);
 cudaError_t launch_score_tc(const nx_cache& c, const nx_params& p, const void* q,
                             const WsLayout& L, char* ws, const ScoreOut& out,
                             int32_t* dev_status, cudaStream_t st, int* launches, bool* used);

@@ -211,7 +211,7 @@ score_simt_kernel(nx_cache c, nx_params p, const float* __restrict__ qbar,
     for (int w = 0; w < WMAX; ++w) tmp[w] = e[w];
     block_reduce<WMAX>(tmp, W, false, red, ssum);
     // walk-row exponentials ew[t] = e[W - H + t]; Gram entries in the fixed pair
-    // layout pair_index(t, u), zero for t or u >= H.
+    // layout pair_index(u, t), u < t, zero for t >= H.
     float ew[kMaxWalk];
 #pragma unroll
     for (int t = 0; t < kMaxWalk; ++t) {
@@ -225,7 +225,7 @@ score_simt_kernel(nx_cache c, nx_params p, const float* __restrict__ qbar,
 #pragma unroll
     for (int t = 0; t < kMaxWalk; ++t)
 #pragma unroll
-      for (int u = t; u < kMaxWalk; ++u) gc[pair_index(t, u)] = ew[t] * ew[u];
+      for (int u = 0; u < t; ++u) gc[pair_index(u, t)] = ew[u] * ew[t];
     block_reduce<kMaxPairs>(gc, kMaxPairs, false, red, sgram);
     for (int i = threadIdx.x; i < W; i += blockDim.x) {
       st[i] = smax[i];
@@ -249,11 +249,11 @@ score_simt_kernel(nx_cache c, nx_params p, const float* __restrict__ qbar,
   }
   __syncthreads();
   for (int k = threadIdx.x; k < kMaxPairs; k += blockDim.x) {
-    int t = 0, u = 0;
-    pair_of(k, t, u);
+    int u = 0, t = 0;
+    pair_of(k, u, t);
     float g = 0.f;
-    if (u < H) {
-      const int wp = W - H + t, wq = W - H + u;
+    if (t < H) {
+      const int wp = W - H + u, wq = W - H + t;
       for (int ch = 0; ch < nch; ++ch) {
         const float* sc = st0 + (long long)ch * stride;
         g += sc[2 * W + k] * expf(sc[wp] - smax[wp]) * expf(sc[wq] - smax[wq]);

@@ -28,9 +28,13 @@
 namespace nx {
 namespace tc {
 
-constexpr int kThreads = 192;          // warps 0-3 epilogue, 4 TMA producer, 5 MMA issuer
+constexpr int kEpiWarps = 8;           // warps 0-7: epilogue (two warpgroups)
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kProducerWarp = kEpiWarps;       // TMA producer
+constexpr int kMmaWarp = kEpiWarps + 1;        // MMA issuer, TMEM owner
+constexpr int kThreads = kEpiThreads + 64;
 constexpr int kTileRows = 128;
-constexpr int kStages = 2;
+constexpr int kStages = 4;
 constexpr long long kWaitLimit = 1LL << 22;   // mbarrier polls before giving up
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -39,6 +43,8 @@ struct Args {
   nx_params p;
   const unsigned char* qimg;   // [slices] shared-memory images of bf16 hi/lo queries
   uint32_t tmem_cols;      // 256 with two CTAs per SM, 512 with one
+  int nbuf;                // TMEM buffers (2: the next chunk's MMAs overlap this epilogue)
+  long long* trace;        // optional phase trace: [grid][kTraceEvents][2] (null: off)
   float* partial;          // [slices][maxc][stride]
   float* fin;              // [slices][3W + kMaxWalk]
   int* arrive;             // [slices] groups of the slice merged
@@ -168,6 +174,30 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// 32 (or 16 when W = 16) consecutive TMEM columns of this thread's lane, one wait.
+template <int N>
+__device__ __forceinline__ void tmem_load(uint32_t taddr, float* v) {
+  uint32_t r[N];
+  tmem_ld16_nowait(taddr, r);
+  if (N == 32) tmem_ld16_nowait(taddr + 16, r + 16);
+  tmem_ld_wait();
+#pragma unroll
+  for (int i = 0; i < N; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
   uint32_t r[16];
 #pragma unroll
@@ -185,14 +215,25 @@ __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// Named barrier of the four epilogue warps (barrier 1; __syncthreads uses barrier 0).
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Named barrier of the epilogue warps (barrier 1; __syncthreads uses barrier 0).
+__device__ __forceinline__ void epi_sync() {
+  asm volatile("bar.sync 1, %0;" ::"r"(kEpiThreads) : "memory");
+}
 
 __device__ __forceinline__ float warp_max(float x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
   return x;
 }
+// Warp maximum of a float through its monotone integer image (one redux instruction).
+__device__ __forceinline__ float warp_max_redux(float x) {
+  uint32_t b = __float_as_uint(x);
+  uint32_t k = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  uint32_t r;
+  asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(k));
+  return __uint_as_float((r & 0x80000000u) ? (r & 0x7FFFFFFFu) : ~r);
+}
+
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
@@ -202,47 +243,69 @@ __device__ __forceinline__ float warp_sum(float x) {
 // ---------------------------------------------------------------------------
 // Merging chunk statistics
 // ---------------------------------------------------------------------------
-constexpr int kGroup = 16;    // records merged at a time
+constexpr int kGroup = 64;    // records merged at a time
 
 // A record holds, for the rows it covers: per window row w the maximum raw logit m_w and
 // sum_j exp((l_wj - m_w)/sqrt(d)) (natural-log units), and per walk-row pair (p, q) the
 // Gram sum_j exp((l_pj - m_p)/sqrt(d)) exp((l_qj - m_q)/sqrt(d)). merge_records combines
-// n <= 16 records (global memory, `stride` floats apart) into one record `dst` of the same
-// form, with the 128 epilogue threads: every value is loaded into shared memory at once
+// n <= kGroup records (global memory, `stride` floats apart) into one record `dst` of the same
+// form, with the epilogue threads: every value is loaded into shared memory at once
 // (independent loads, one round trip), then combined in a fixed order.
 template <int W>
 __device__ __forceinline__ void merge_records(const float* src, int n, int stride, float* dst,
                                               float* stage, int H, float cl2) {
   constexpr int R = 2 * W + kMaxPairs;
+  constexpr int PARTS = kEpiThreads / W;       // threads per window row
   const int tid = threadIdx.x;
-  for (int idx = tid; idx < n * R; idx += 128) {
+  for (int idx = tid; idx < n * R; idx += kEpiThreads) {
     const int i = idx / R, f = idx - i * R;
     stage[idx] = __ldcg(&src[(long long)i * stride + f]);
   }
-  float* sM = stage + kGroup * R;      // merged maxima (the Gram step needs them)
+  float* sM = stage + kGroup * R;      // merged maxima (W <= 64 floats)
+  float* part = sM + 64 + R;           // [PARTS][W] partial results (after the dst slot)
+  epi_sync();
+  const int w = tid % W, pt = tid / W;
+  float m = -INFINITY;
+  for (int i = pt; i < n; i += PARTS) m = fmaxf(m, stage[i * R + w]);
+  part[pt * W + w] = m;
   epi_sync();
   if (tid < W) {
-    float M = -INFINITY;
-    for (int i = 0; i < n; ++i) M = fmaxf(M, stage[i * R + tid]);
-    float Z = 0.f;
-    for (int i = 0; i < n; ++i) Z += stage[i * R + W + tid] * exp2f((stage[i * R + tid] - M) * cl2);
+    float M = part[tid];
+    for (int q = 1; q < PARTS; ++q) M = fmaxf(M, part[q * W + tid]);
     sM[tid] = M;
-    dst[tid] = M;
-    dst[W + tid] = Z;
   }
   epi_sync();
-  if (tid < kMaxPairs) {
-    int t, u;
-    pair_of(tid, t, u);
-    float g = 0.f;
-    if (u < H) {
-      const int wp = W - H + t, wq = W - H + u;
-      for (int i = 0; i < n; ++i) {
-        const float* r = stage + i * R;
-        g += r[2 * W + tid] * exp2f(((r[wp] - sM[wp]) + (r[wq] - sM[wq])) * cl2);
-      }
+  const float Mw = sM[w];
+  float z = 0.f;
+  for (int i = pt; i < n; i += PARTS) z += stage[i * R + W + w] * exp2f((stage[i * R + w] - Mw) * cl2);
+  part[pt * W + w] = z;
+  // Gram pairs: threads split over (pair, part of the records)
+  constexpr int GP = kEpiThreads / kMaxPairs;  // 9 parts for 28 pairs
+  float g = 0.f;
+  int pu = 0, pt2 = 0, gi = tid % kMaxPairs;
+  const int gpart = tid / kMaxPairs;
+  pair_of(gi, pu, pt2);
+  if (gpart < GP && pt2 < H) {
+    const int wp = W - H + pu, wq = W - H + pt2;
+    const float mp = sM[wp], mq = sM[wq];
+    for (int i = gpart; i < n; i += GP) {
+      const float* r = stage + i * R;
+      g += r[2 * W + gi] * exp2f(((r[wp] - mp) + (r[wq] - mq)) * cl2);
     }
-    dst[2 * W + tid] = g;
+  }
+  float* gpartial = part + PARTS * W;          // [GP][kMaxPairs]
+  if (gpart < GP) gpartial[gpart * kMaxPairs + gi] = g;
+  epi_sync();
+  if (tid < W) {
+    float Z = 0.f;
+    for (int q = 0; q < PARTS; ++q) Z += part[q * W + tid];
+    dst[tid] = sM[tid];
+    dst[W + tid] = Z;
+  } else if (tid >= 64 && tid < 64 + kMaxPairs) {
+    const int k = tid - 64;
+    float G = 0.f;
+    for (int q = 0; q < GP; ++q) G += gpartial[q * kMaxPairs + k];
+    dst[2 * W + k] = G;
   }
   epi_sync();
 }
@@ -256,58 +319,476 @@ struct Smem {
   static constexpr int kRegionA = kTileRows * 128;        // one column block of a K tile
   static constexpr int kTileBytes = KB * kRegionA;
   static constexpr int kRegionB = W * 128;                // one column block of Qbar
-  static constexpr int kOffK = 0;
-  static constexpr int kOffQ = kStages * kTileBytes;      // [hi, lo][KB][kRegionB]
-  static constexpr int kOffBar = kOffQ + 2 * KB * kRegionB;
-  static constexpr int kOffMisc = kOffBar + 64;           // tmem slot + control words
   static constexpr int kQBytes = 2 * KB * kRegionB;       // hi + lo query image
-  static constexpr int kOffRed = kOffMisc + 64;           // [4][W + kMaxPairs] floats
-  static constexpr int kOffCoef = kOffRed + 4 * (W + kMaxPairs) * 4;  // mc[W] ca[W] cc[8]
   static constexpr int kRec = 2 * W + kMaxPairs;          // floats of one chunk record
-  static constexpr int kOffStage = kOffCoef + (2 * W + kMaxWalk) * 4;  // [16][kRec] + M Z G
-  // staging for 16 records, the merged maxima (<= 64 floats), then one merged record
-  static constexpr int kBytes = kOffStage + (16 * kRec + 64 + kRec) * 4;
+  static constexpr int kRedStride = W + kMaxPairs;        // one warp's partial reductions
+  static constexpr int kOffK = 0;
+  static constexpr int kOffQ = kStages * kTileBytes;
+  static constexpr int kOffBar = kOffQ + kQBytes;         // 16 mbarriers
+  static constexpr int kOffMisc = kOffBar + 128;          // tmem slot + control words
+  static constexpr int kOffRed = kOffMisc + 64;           // [kEpiWarps][kRedStride]
+  static constexpr int kOffMc = kOffRed + kEpiWarps * kRedStride * 4;   // [2][W] chunk maxima
+  static constexpr int kOffCa = kOffMc + 2 * W * 4;       // [W] a coefficients
+  static constexpr int kOffCc = kOffCa + W * 4;           // [kMaxWalk] walk coefficients
+  // merge staging: [kGroup][kRec] records, 64 maxima, one merged record, partial sums
+  static constexpr int kOffStage = kOffCc + kMaxWalk * 4;
+  static constexpr int kBytes =
+      kOffStage + (kGroup * kRec + 64 + kRec + kEpiThreads + kEpiThreads) * 4;
   static constexpr int kAlloc = kBytes + 1024;            // slack for 1024-byte alignment
 };
 
+// Next chunk id >= id (stepping by the grid) that has work, or -1. Every role of a CTA
+// walks the same sequence.
+__device__ __forceinline__ long long next_chunk(const Args& A, long long id, int chunk_rows) {
+  for (; id < A.total_ids; id += gridDim.x) {
+    const int slice = (int)(id / A.maxc);
+    const int k = (int)(id % A.maxc);
+    if (A.newlen[slice] < 0) continue;
+    const int T = A.c.lens[slice];
+    if (k * chunk_rows >= T) continue;
+    return id;
+  }
+  return -1;
+}
+
+constexpr int kTraceEvents = 1024;
+
+__device__ __forceinline__ long long global_ns() {
+  long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Phase trace (diagnostics, off unless a buffer is installed): event e of this CTA gets
+// (tag, globaltimer ns).
+__device__ __forceinline__ void trace_ev(const Args& A, int& n, int tag) {
+  if (A.trace && n < kTraceEvents) {
+    long long* t = A.trace + ((long long)blockIdx.x * kTraceEvents + n) * 2;
+    t[0] = tag;
+    t[1] = global_ns();
+    ++n;
+  }
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// One chunk as the epilogue sees it.
+struct Chunk {
+  int slice, k, T, nchunks, j0, ntiles, l, s, h;
+  uint32_t b;          // TMEM buffer
+  uint32_t use;        // how many times this buffer was used before
+};
+
+__device__ __forceinline__ Chunk decode_chunk(const Args& A, long long id, int chunk_rows,
+                                              uint32_t cc, int nbuf) {
+  Chunk ch;
+  ch.slice = (int)(id / A.maxc);
+  ch.k = (int)(id % A.maxc);
+  ch.T = A.c.lens[ch.slice];
+  ch.nchunks = (ch.T + chunk_rows - 1) / chunk_rows;
+  ch.j0 = ch.k * chunk_rows;
+  ch.ntiles = min(A.tiles_per_chunk, (ch.T - ch.j0 + kTileRows - 1) / kTileRows);
+  slice_coords(A.c, ch.slice, ch.l, ch.s, ch.h);
+  ch.b = cc % nbuf;
+  ch.use = cc / nbuf;
+  return ch;
+}
+
+// Epilogue state shared by the passes.
 template <int W, int D>
-__global__ void __launch_bounds__(kThreads, 2)
+struct Epi {
+  const Args& A;
+  uint8_t* sm;
+  uint32_t tmem;
+  uint32_t buf_cols;
+  float cl2;
+  int H;
+  int warp, lane, wg;   // wg: warpgroup, which takes every other tile of a chunk
+  int nev = 0;          // trace events written (thread 0)
+  __device__ Epi(const Args& a, uint8_t* s, uint32_t t, uint32_t bc, float c2, int h)
+      : A(a), sm(s), tmem(t), buf_cols(bc), cl2(c2), H(h) {
+    warp = threadIdx.x >> 5;
+    lane = threadIdx.x & 31;
+    wg = warp >> 2;
+  }
+  __device__ float* red() { return reinterpret_cast<float*>(sm + Smem<W, D>::kOffRed); }
+  __device__ float* mc(uint32_t b) {
+    return reinterpret_cast<float*>(sm + Smem<W, D>::kOffMc) + b * W;
+  }
+  __device__ float* ca() { return reinterpret_cast<float*>(sm + Smem<W, D>::kOffCa); }
+  __device__ float* cc() { return reinterpret_cast<float*>(sm + Smem<W, D>::kOffCc); }
+  __device__ uint32_t lane_base(const Chunk& ch) {
+    return tmem + ((uint32_t)((warp & 3) * 32) << 16) + ch.b * buf_cols;
+  }
+  __device__ bool row_valid(const Chunk& ch, int t) {
+    return ch.j0 + t * kTileRows + (warp & 3) * 32 + lane < ch.T;
+  }
+
+  // Combine per-warp partials red[warp][i], i < n, over the epilogue warps.
+  __device__ float combine(int i, bool is_max) {
+    constexpr int RS = Smem<W, D>::kRedStride;
+    float v = red()[i];
+    for (int w8 = 1; w8 < kEpiWarps; ++w8)
+      v = is_max ? fmaxf(v, red()[w8 * RS + i]) : v + red()[w8 * RS + i];
+    return v;
+  }
+
+  // Passes 1a/1b: chunk maxima, e = exp((l - max)/sqrt(d)) written back to TMEM, chunk
+  // sums and the walk-row Gram; the record goes to global memory.
+  template <int HT>
+  __device__ void stats(const Chunk& ch) {
+    constexpr int RS = Smem<W, D>::kRedStride;
+    constexpr int NB = (W >= 32) ? 32 : 16;
+    const uint32_t lb = lane_base(ch);
+    float* m = mc(ch.b);
+    float mx[W];
+#pragma unroll
+    for (int w = 0; w < W; ++w) mx[w] = -INFINITY;
+    for (int t = wg; t < ch.ntiles; t += 2) {
+      const bool valid = row_valid(ch, t);
+#pragma unroll
+      for (int cb = 0; cb < W; cb += NB) {
+        float v[NB];
+        tmem_load<NB>(lb + t * W + cb, v);
+#pragma unroll
+        for (int i = 0; i < NB; ++i) mx[cb + i] = fmaxf(mx[cb + i], valid ? v[i] : -INFINITY);
+      }
+    }
+    if (threadIdx.x == 0) trace_ev(A, nev, 10);
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      const float x = warp_max_redux(mx[w]);
+      if (lane == 0) red()[warp * RS + w] = x;
+    }
+    epi_sync();
+    if (threadIdx.x < W) m[threadIdx.x] = combine(threadIdx.x, true);
+    epi_sync();
+    if (threadIdx.x == 0) trace_ev(A, nev, 11);
+    float z[W], gp[kMaxPairs];
+#pragma unroll
+    for (int w = 0; w < W; ++w) z[w] = 0.f;
+#pragma unroll
+    for (int i = 0; i < kMaxPairs; ++i) gp[i] = 0.f;
+    for (int t = wg; t < ch.ntiles; t += 2) {
+      const bool valid = row_valid(ch, t);
+      float ew[kMaxWalk];
+#pragma unroll
+      for (int cb = 0; cb < W; cb += NB) {
+        float v[NB];
+        tmem_load<NB>(lb + t * W + cb, v);
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+          const float e = valid ? exp2f((v[i] - m[cb + i]) * cl2) : 0.f;
+          v[i] = e;
+          z[cb + i] += e;
+        }
+        tmem_st16(lb + t * W + cb, v);
+        if (NB == 32) tmem_st16(lb + t * W + cb + 16, v + 16);
+        if (cb + NB == W) {   // the walk rows W-H .. W-1 are the last H columns
+          if (HT >= 0) {
+#pragma unroll
+            for (int tt = 0; tt < kMaxWalk; ++tt) ew[tt] = (tt < HT) ? v[NB - HT + tt] : 0.f;
+          } else {
+#pragma unroll
+            for (int tt = 0; tt < kMaxWalk; ++tt) {
+              float x = 0.f;
+#pragma unroll
+              for (int i = NB - kMaxWalk; i < NB; ++i)
+                if (tt < H && i == NB - H + tt) x = v[i];
+              ew[tt] = x;
+            }
+          }
+        }
+      }
+      if (HT >= 0) {
+#pragma unroll
+        for (int tt = 1; tt < (HT > 0 ? HT : 1); ++tt)
+#pragma unroll
+          for (int uu = 0; uu < tt; ++uu) gp[pair_index(uu, tt)] += ew[uu] * ew[tt];
+      } else {
+#pragma unroll
+        for (int tt = 1; tt < kMaxWalk; ++tt)
+#pragma unroll
+          for (int uu = 0; uu < tt; ++uu) gp[pair_index(uu, tt)] += ew[uu] * ew[tt];
+      }
+    }
+    tmem_st_wait();
+    if (threadIdx.x == 0) trace_ev(A, nev, 12);
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      const float x = warp_sum(z[w]);
+      if (lane == 0) red()[warp * RS + w] = x;
+    }
+    constexpr int NP = (HT >= 0) ? (HT * (HT - 1) / 2 > 0 ? HT * (HT - 1) / 2 : 0) : kMaxPairs;
+#pragma unroll
+    for (int i = 0; i < kMaxPairs; ++i) {
+      const float x = (i < NP) ? warp_sum(gp[i]) : 0.f;
+      if (lane == 0) red()[warp * RS + W + i] = x;
+    }
+    epi_sync();
+    float* rec = A.partial + ((long long)ch.slice * A.maxc + ch.k) * A.stride;
+    if (threadIdx.x < W) {
+      rec[threadIdx.x] = m[threadIdx.x];                     // chunk max (raw)
+      rec[W + threadIdx.x] = combine(threadIdx.x, false);    // sum relative to it
+    } else if (threadIdx.x < W + kMaxPairs) {
+      rec[W + threadIdx.x] = combine(threadIdx.x, false);    // Gram entry
+    }
+  }
+
+  // Publish the chunk's record; the last chunk of a group merges the group, the last group
+  // of the slice merges the groups and publishes the coefficients. Never waits.
+  __device__ void publish(const Chunk& ch, bool ok) {
+    using S = Smem<W, D>;
+    int* ctl = reinterpret_cast<int*>(sm + S::kOffMisc + 16);
+    const int ngs = (ch.nchunks + kGroup - 1) / kGroup;
+    const int grp = ch.k / kGroup;
+    const int gsize = min(kGroup, ch.nchunks - grp * kGroup);
+    float* stage = reinterpret_cast<float*>(sm + S::kOffStage);
+    float* merged = stage + kGroup * S::kRec;
+    // every epilogue thread's record stores precede the barrier; thread 0 then fences and
+    // signals (release), and fences again after a successful count (acquire)
+    epi_sync();
+    if (threadIdx.x == 0) {
+      ctl[0] = 0;
+      if (!ok) {
+        ctl[1] = 1;
+      } else {
+        __threadfence();
+        const int prev = atomicAdd(&A.garrive[(long long)ch.slice * A.ngroups + grp], 1);
+        ctl[0] = (prev == gsize - 1) ? 1 : 0;
+        if (ctl[0]) __threadfence();
+      }
+    }
+    epi_sync();
+    if (ctl[0] && ngs > 1) {
+      float* grec = A.grec + ((long long)ch.slice * A.ngroups + grp) * A.stride;
+      merge_records<W>(A.partial + ((long long)ch.slice * A.maxc + grp * kGroup) * A.stride,
+                       gsize, A.stride, grec, stage, H, cl2);
+      if (threadIdx.x == 0) {
+        __threadfence();
+        const int prev = atomicAdd(&A.arrive[ch.slice], 1);
+        ctl[0] = (prev == ngs - 1) ? 2 : 0;
+        if (ctl[0]) __threadfence();
+      }
+      epi_sync();
+    } else if (ctl[0]) {
+      if (threadIdx.x == 0) ctl[0] = 2;         // one group: its last chunk merges directly
+      epi_sync();
+    }
+    if (ctl[0] == 2) {
+      float* fin = A.fin + (long long)ch.slice * (3 * W + kMaxWalk);
+      float* rec = merged + 64;
+      if (ngs > 1)
+        merge_records<W>(A.grec + (long long)ch.slice * A.ngroups * A.stride, ngs, A.stride, rec,
+                         stage, H, cl2);
+      else
+        merge_records<W>(A.partial + (long long)ch.slice * A.maxc * A.stride, gsize, A.stride,
+                         rec, stage, H, cl2);
+      if (threadIdx.x == 0) {
+        // Eq. (4) in rank-1 form on <P_u, P_t> = Gram / (Z_u Z_t)
+        float gam[kMaxWalk], gsum = 0.f;
+        for (int t = 0; t < H; ++t) {
+          float g = 1.f;
+          for (int u = 0; u < t; ++u)
+            g += gam[u] * rec[2 * W + pair_index(u, t)] /
+                 (rec[W + (W - H + u)] * rec[W + (W - H + t)]);
+          gam[t] = g;
+          gsum += g;
+        }
+        // ||C||_1 = sum_t gamma_t since every row P sums to one
+        for (int t = 0; t < kMaxWalk; ++t)
+          fin[3 * W + t] = (t < H) ? gam[t] / (gsum * rec[W + (W - H + t)]) : 0.f;
+      }
+      if (threadIdx.x < W) {
+        const int w = threadIdx.x;
+        fin[w] = rec[w];                                      // raw max
+        fin[W + w] = rec[W + w];                              // normaliser
+        fin[2 * W + w] = 1.0f / ((float)W * rec[W + w]);
+      }
+      epi_sync();
+      if (threadIdx.x == 0) {
+        __threadfence();
+        st_release(&A.ready[ch.slice], 1);
+        trace_ev(A, nev, 7 + 1000 * (ch.slice + 1));
+      }
+    }
+  }
+
+  // Wait for the slice's coefficients, then a, c~, w and the order key of every row.
+  template <int HT>
+  __device__ bool emit(const Chunk& ch) {
+    using S = Smem<W, D>;
+    constexpr int NB = (W >= 32) ? 32 : 16;
+    int* ctl = reinterpret_cast<int*>(sm + S::kOffMisc + 16);
+    const nx_cache& c = A.c;
+    const nx_params& p = A.p;
+    // the positions of this thread's rows (needed for the keys), loaded before waiting
+    constexpr int kMaxRows = 8;
+    int32_t posv[kMaxRows];
+#pragma unroll
+    for (int r = 0; r < kMaxRows; ++r) {
+      const int t = wg + 2 * r;
+      const int j = ch.j0 + t * kTileRows + (warp & 3) * 32 + lane;
+      posv[r] = (t < ch.ntiles && j < ch.T && (A.out.flags & kEmitKeys))
+                    ? __ldg(&c.pos[row_of(c, ch.l, ch.s, ch.h, j)]) : 0;
+    }
+    if (threadIdx.x == 0 && !ctl[1])
+      if (!wait_at_least(&A.ready[ch.slice], 1, A.dev_status)) ctl[1] = 1;
+    epi_sync();
+    if (threadIdx.x == 0) trace_ev(A, nev, 5 + 1000 * (ch.slice + 1));
+    if (ctl[1]) return false;
+    const float* fin = A.fin + (long long)ch.slice * (3 * W + kMaxWalk);
+    const float* m = mc(ch.b);
+    if (threadIdx.x < W) {
+      const int w = threadIdx.x;
+      const float shift = exp2f((m[w] - __ldcg(&fin[w])) * cl2);
+      ca()[w] = __ldcg(&fin[2 * W + w]) * shift;
+      if (w >= W - H) cc()[w - (W - H)] = __ldcg(&fin[3 * W + (w - (W - H))]) * shift;
+    }
+    if (ch.k == 0 && (A.out.flags & kEmitStats) && threadIdx.x < W) {
+      const int w = threadIdx.x;
+      A.out.row_stats[((long long)ch.slice * W + w) * 2] = __ldcg(&fin[w]) * rsqrtf((float)D);
+      A.out.row_stats[((long long)ch.slice * W + w) * 2 + 1] = __ldcg(&fin[W + w]);
+    }
+    epi_sync();
+    if (threadIdx.x == 0) trace_ev(A, nev, 6);
+    const uint32_t lb = lane_base(ch);
+    const uint32_t head_id = (uint32_t)((p.layer_id_base + ch.l) * c.kv_heads + ch.h);
+    const uint32_t seq_id = (uint32_t)(p.seq_id_base + ch.s);
+    const float* sca = ca();
+    const float* scc = cc();
+#pragma unroll
+    for (int r = 0; r < kMaxRows; ++r) {
+      const int t = wg + 2 * r;
+      if (t >= ch.ntiles) break;
+      const int j = ch.j0 + t * kTileRows + (warp & 3) * 32 + lane;
+      float a = 0.f, ct = 0.f;
+#pragma unroll
+      for (int cb = 0; cb < W; cb += NB) {
+        float v[NB];
+        tmem_load<NB>(lb + t * W + cb, v);
+#pragma unroll
+        for (int i = 0; i < NB; ++i) a = fmaf(v[i], sca[cb + i], a);
+        if (cb + NB == W) {
+          if (HT >= 0) {
+#pragma unroll
+            for (int tt = 0; tt < (HT > 0 ? HT : 0); ++tt) ct = fmaf(v[NB - HT + tt], scc[tt], ct);
+          } else {
+#pragma unroll
+            for (int i = NB - kMaxWalk; i < NB; ++i)
+              if (i >= NB - H) ct = fmaf(v[i], scc[i - (NB - H)], ct);
+          }
+        }
+      }
+      if (j < ch.T) {
+        const float sj = a + p.lambda * ct;
+        const float ramp = (ch.T > 1) ? (float)j / (float)(ch.T - 1) : 0.f;
+        const float wj = sj + p.eps_tie * ramp;
+        const long long o = (long long)ch.slice * c.capacity + j;
+        if (A.out.flags & kEmitA) A.out.a[o] = a;
+        if (A.out.flags & kEmitC) A.out.ctilde[o] = ct;
+        if (A.out.flags & kEmitW) A.out.w[o] = wj;
+        if (A.out.flags & kEmitKeys) {
+          uint32_t key = kForcedKey;
+          if (!(j < p.n_sink || j >= ch.T - p.n_recent))
+            key = candidate_key(wj, posv[r], p, head_id, seq_id);
+          A.out.keys[o] = key;
+        }
+      }
+    }
+    return true;
+  }
+
+  // The epilogue loop. With two TMEM buffers it is software-pipelined: chunk c+1's
+  // statistics are computed and published before chunk c waits for its slice.
+  template <int HT>
+  __device__ void run(uint64_t* bar_tfull, uint64_t* bar_tempty, int chunk_rows, int nbuf) {
+    using S = Smem<W, D>;
+    int* ctl = reinterpret_cast<int*>(sm + S::kOffMisc + 16);
+    Chunk prev;
+    bool have_prev = false;
+    uint32_t cnt = 0;
+    auto finish = [&](const Chunk& ch) -> bool {
+      if (threadIdx.x == 0) trace_ev(A, nev, 3 + 1000 * (ch.slice + 1));
+      const bool ok = emit<HT>(ch);
+      tc_fence_before();
+      epi_sync();
+      if (threadIdx.x == 0) {
+        trace_ev(A, nev, 4);
+        mbar_arrive(&bar_tempty[ch.b]);
+        if (!ok) ctl[1] = 1;
+      }
+      return ok;
+    };
+    for (long long id = next_chunk(A, blockIdx.x, chunk_rows); id >= 0;
+         id = next_chunk(A, id + gridDim.x, chunk_rows), ++cnt) {
+      if (ctl[1]) break;
+      const Chunk ch = decode_chunk(A, id, chunk_rows, cnt, nbuf);
+      if (threadIdx.x == 0) trace_ev(A, nev, 100 + ch.k);
+      const bool ok = mbar_wait(&bar_tfull[ch.b], ch.use & 1, A.dev_status);
+      tc_fence_after();
+      if (threadIdx.x == 0) trace_ev(A, nev, 1);
+      if (ok) stats<HT>(ch);
+      if (threadIdx.x == 0) trace_ev(A, nev, 2 + 1000 * (ch.slice + 1));
+      publish(ch, ok);
+      if (!ok) break;
+      if (nbuf == 1) {
+        if (!finish(ch)) break;
+      } else {
+        if (have_prev && !finish(prev)) break;
+        prev = ch;
+        have_prev = true;
+      }
+    }
+    if (nbuf != 1 && have_prev && !ctl[1]) finish(prev);
+  }
+};
+
+// 10 warps per CTA: one SM sub-partition holds 3 of them, so the 16K-register share of a
+// sub-partition caps a thread at 168 registers.
+template <int W, int D>
+__global__ void __launch_bounds__(kThreads, 1)
 score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
   using S = Smem<W, D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
-  uint64_t* bar_full = reinterpret_cast<uint64_t*>(sm + S::kOffBar);
-  uint64_t* bar_empty = bar_full + kStages;
-  uint64_t* bar_mma = bar_empty + kStages;
-  uint64_t* bar_q = bar_mma + 1;
+  uint64_t* bar_full = reinterpret_cast<uint64_t*>(sm + S::kOffBar);   // [kStages]
+  uint64_t* bar_empty = bar_full + kStages;                           // [kStages]
+  uint64_t* bar_tfull = bar_empty + kStages;                          // [2] TMEM buffer ready
+  uint64_t* bar_tempty = bar_tfull + 2;                               // [2] TMEM buffer free
+  uint64_t* bar_qfull = bar_tempty + 2;
+  uint64_t* bar_qempty = bar_qfull + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S::kOffMisc);
-  int* ctl = reinterpret_cast<int*>(sm + S::kOffMisc + 16);   // [0] last-arriver, [1] abort
-  float* red = reinterpret_cast<float*>(sm + S::kOffRed);
-  float* s_mc = reinterpret_cast<float*>(sm + S::kOffCoef);   // chunk maxima (raw logits)
-  float* s_ca = s_mc + W;                                     // per-row a coefficients
-  float* s_cc = s_ca + W;                                     // walk coefficients
+  int* ctl = reinterpret_cast<int*>(sm + S::kOffMisc + 16);   // [0] merge role, [1] abort
 
   const nx_cache& c = A.c;
-  const nx_params& p = A.p;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int H = p.walk_len;
   const float cl2 = kLog2e * rsqrtf((float)D);   // raw accumulator -> log2 units
   constexpr uint32_t kIdesc = idesc_bf16<W>();
   const int chunk_rows = A.tiles_per_chunk * kTileRows;
+  const int nbuf = A.nbuf;
+  const uint32_t buf_cols = A.tmem_cols / (uint32_t)nbuf;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bar_full[s], 1);
-      mbar_init(&bar_empty[s], 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&bar_full[i], 1);
+      mbar_init(&bar_empty[i], 1);
     }
-    mbar_init(bar_mma, 1);
-    mbar_init(bar_q, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_tfull[i], 1);
+      mbar_init(&bar_tempty[i], 1);
+    }
+    mbar_init(bar_qfull, 1);
+    mbar_init(bar_qempty, 1);
+    ctl[0] = 0;
     ctl[1] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
                  "r"(A.tmem_cols));
@@ -317,42 +798,32 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  volatile int* abort_flag = ctl + 1;
 
-  uint32_t it = 0;          // tiles streamed by this CTA (stage/phase bookkeeping)
-  uint32_t chunks_done = 0;
-  uint32_t q_loads = 0;     // query images fetched (bar_q phase bookkeeping)
-  int prev_slice = -1;
-
-  for (long long id = blockIdx.x; id < A.total_ids; id += gridDim.x) {
-    const int slice = (int)(id / A.maxc);
-    const int k = (int)(id % A.maxc);
-    if (A.newlen[slice] < 0) continue;
-    const int T = c.lens[slice];
-    const int nchunks = (T + chunk_rows - 1) / chunk_rows;
-    if (k >= nchunks) continue;
-    if (ctl[1]) break;                       // an earlier wait gave up
-    int l, s, h;
-    slice_coords(c, slice, l, s, h);
-    const int j0 = k * chunk_rows;
-    const int ntiles = min(A.tiles_per_chunk, (T - j0 + kTileRows - 1) / kTileRows);
-
-    // the slice's query image is fetched by the producer below when the slice changes;
-    // the previous chunk's MMAs (its only readers) completed before the last barrier
-    const bool new_q = slice != prev_slice;
-    prev_slice = slice;
-    __syncthreads();
-
-    if (warp == 4) {
-      // ---------------- TMA producer ----------------
-      if (lane == 0) {
-        if (new_q) {
-          mbar_expect_tx(bar_q, S::kQBytes);
+  if (warp == kProducerWarp) {
+    // =================== TMA producer: query images and K tiles ===================
+    if (lane == 0) {
+      uint32_t u = 0, qn = 0;
+      int prev_slice = -1;
+      for (long long id = next_chunk(A, blockIdx.x, chunk_rows); id >= 0 && !*abort_flag;
+           id = next_chunk(A, id + gridDim.x, chunk_rows)) {
+        const int slice = (int)(id / A.maxc), k = (int)(id % A.maxc);
+        const int T = c.lens[slice];
+        int l, s, h;
+        slice_coords(c, slice, l, s, h);
+        const int j0 = k * chunk_rows;
+        const int ntiles = min(A.tiles_per_chunk, (T - j0 + kTileRows - 1) / kTileRows);
+        if (slice != prev_slice) {
+          if (qn > 0 && !mbar_wait(bar_qempty, (qn - 1) & 1, A.dev_status)) { *abort_flag = 1; break; }
+          mbar_expect_tx(bar_qfull, S::kQBytes);
           bulk_load(smem_u32(sm + S::kOffQ), A.qimg + (long long)slice * S::kQBytes, S::kQBytes,
-                    bar_q);
+                    bar_qfull);
+          ++qn;
+          prev_slice = slice;
         }
-        for (int t = 0; t < ntiles; ++t) {
-          const uint32_t u = it + t, st = u % kStages, ph = (u / kStages) & 1;
-          if (!mbar_wait(&bar_empty[st], ph ^ 1, A.dev_status)) { ctl[1] = 1; break; }
+        for (int t = 0; t < ntiles; ++t, ++u) {
+          const uint32_t st = u % kStages, ph = (u / kStages) & 1;
+          if (!mbar_wait(&bar_empty[st], ph ^ 1, A.dev_status)) { *abort_flag = 1; break; }
           const uint32_t dst = smem_u32(sm + S::kOffK + st * S::kTileBytes);
           const int r0 = j0 + t * kTileRows;
           if (c.page_size == 0) {
@@ -375,18 +846,34 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
           }
         }
       }
-    } else if (warp == 5) {
-      // ---------------- MMA issuer ----------------
-      if (lane == 0) {
+    }
+  } else if (warp == kMmaWarp) {
+    // =================== MMA issuer ===================
+    if (lane == 0) {
+      uint32_t u = 0, qn = 0, cc = 0;
+      int prev_slice = -1;
+      const uint32_t qa = smem_u32(sm + S::kOffQ);
+      for (long long id = next_chunk(A, blockIdx.x, chunk_rows); id >= 0 && !*abort_flag;
+           id = next_chunk(A, id + gridDim.x, chunk_rows), ++cc) {
+        const int slice = (int)(id / A.maxc), k = (int)(id % A.maxc);
+        const int T = c.lens[slice];
+        const int j0 = k * chunk_rows;
+        const int ntiles = min(A.tiles_per_chunk, (T - j0 + kTileRows - 1) / kTileRows);
+        const uint32_t b = cc % nbuf, use = cc / nbuf;
+        if (!mbar_wait(&bar_tempty[b], (use & 1) ^ 1, A.dev_status)) { *abort_flag = 1; break; }
         tc_fence_after();
-        const uint32_t qa = smem_u32(sm + S::kOffQ);
-        if (new_q && !mbar_wait(bar_q, q_loads & 1, A.dev_status)) ctl[1] = 1;
-        for (int t = 0; t < ntiles && !ctl[1]; ++t) {
-          const uint32_t u = it + t, st = u % kStages, ph = (u / kStages) & 1;
-          if (!mbar_wait(&bar_full[st], ph, A.dev_status)) { ctl[1] = 1; break; }
+        if (slice != prev_slice) {
+          if (!mbar_wait(bar_qfull, qn & 1, A.dev_status)) { *abort_flag = 1; break; }
+          ++qn;
+          prev_slice = slice;
+        }
+        bool fail = false;
+        for (int t = 0; t < ntiles; ++t, ++u) {
+          const uint32_t st = u % kStages, ph = (u / kStages) & 1;
+          if (!mbar_wait(&bar_full[st], ph, A.dev_status)) { fail = true; break; }
           tc_fence_after();
           const uint32_t ka = smem_u32(sm + S::kOffK + st * S::kTileBytes);
-          const uint32_t dt = tmem + (uint32_t)(t * W);
+          const uint32_t dt = tmem + b * buf_cols + (uint32_t)(t * W);
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
 #pragma unroll
@@ -401,226 +888,26 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
           }
           mma_commit(&bar_empty[st]);      // the stage's smem is free once these finish
         }
-        mma_commit(bar_mma);               // all tiles of the chunk are in TMEM
+        if (fail) { *abort_flag = 1; break; }
+        mma_commit(&bar_tfull[b]);         // the chunk's logits are in TMEM buffer b
+        const long long nid = next_chunk(A, id + gridDim.x, chunk_rows);
+        if (nid >= 0 && (int)(nid / A.maxc) != slice)
+          mma_commit(bar_qempty);          // the query image may be replaced after these
       }
-    } else {
-      // ---------------- epilogue: warps 0-3, TMEM lane = row ----------------
-      const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-      bool ok = mbar_wait(bar_mma, chunks_done & 1, A.dev_status);
-      tc_fence_after();
-      // pass 1a: chunk maxima of the raw accumulators
-      float mx[W];
-#pragma unroll
-      for (int w = 0; w < W; ++w) mx[w] = -INFINITY;
-      for (int t = 0; t < ntiles && ok; ++t) {
-        const bool valid = j0 + t * kTileRows + warp * 32 + lane < T;
-#pragma unroll
-        for (int cb = 0; cb < W; cb += 16) {
-          float v[16];
-          tmem_ld16(lane_base + t * W + cb, v);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) mx[cb + i] = fmaxf(mx[cb + i], valid ? v[i] : -INFINITY);
-        }
-      }
-#pragma unroll
-      for (int w = 0; w < W; ++w) {
-        const float m = warp_max(mx[w]);
-        if (lane == 0) red[warp * (W + kMaxPairs) + w] = m;
-      }
-      epi_sync();
-      if (threadIdx.x < W) {
-        float m = red[threadIdx.x];
-        for (int q4 = 1; q4 < 4; ++q4) m = fmaxf(m, red[q4 * (W + kMaxPairs) + threadIdx.x]);
-        s_mc[threadIdx.x] = m;
-      }
-      epi_sync();
-      // pass 1b: e = exp((l - max)/sqrt(d)) back into TMEM, chunk sums and walk Gram
-      float z[W], gp[kMaxPairs];
-#pragma unroll
-      for (int w = 0; w < W; ++w) z[w] = 0.f;
-#pragma unroll
-      for (int i = 0; i < kMaxPairs; ++i) gp[i] = 0.f;
-      for (int t = 0; t < ntiles && ok; ++t) {
-        const bool valid = j0 + t * kTileRows + warp * 32 + lane < T;
-        float ew[kMaxWalk];
-#pragma unroll
-        for (int cb = 0; cb < W; cb += 16) {
-          float v[16];
-          tmem_ld16(lane_base + t * W + cb, v);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float e = valid ? exp2f((v[i] - s_mc[cb + i]) * cl2) : 0.f;
-            v[i] = e;
-            z[cb + i] += e;
-          }
-          tmem_st16(lane_base + t * W + cb, v);
-          if (cb + 16 >= W) {   // the walk rows W-H .. W-1 lie in the last 16 columns
-#pragma unroll
-            for (int tt = 0; tt < kMaxWalk; ++tt) {
-              float x = 0.f;
-#pragma unroll
-              for (int i = 0; i < 16; ++i)
-                if (tt < H && cb + i == W - H + tt) x = v[i];
-              ew[tt] = x;
-            }
-          }
-        }
-#pragma unroll
-        for (int tt = 0; tt < kMaxWalk; ++tt)
-#pragma unroll
-          for (int uu = tt; uu < kMaxWalk; ++uu) gp[pair_index(tt, uu)] += ew[tt] * ew[uu];
-      }
-      tmem_st_wait();
-#pragma unroll
-      for (int w = 0; w < W; ++w) {
-        const float v = warp_sum(z[w]);
-        if (lane == 0) red[warp * (W + kMaxPairs) + w] = v;
-      }
-#pragma unroll
-      for (int i = 0; i < kMaxPairs; ++i) {
-        const float v = warp_sum(gp[i]);
-        if (lane == 0) red[warp * (W + kMaxPairs) + W + i] = v;
-      }
-      epi_sync();
-      float* rec = A.partial + ((long long)slice * A.maxc + k) * A.stride;
-      if (threadIdx.x < W + kMaxPairs) {
-        float v = 0.f;
-        for (int q4 = 0; q4 < 4; ++q4) v += red[q4 * (W + kMaxPairs) + threadIdx.x];
-        if (threadIdx.x < W) {
-          rec[threadIdx.x] = s_mc[threadIdx.x];     // chunk max (raw)
-          rec[W + threadIdx.x] = v;                 // chunk sum relative to that max
-        } else {
-          rec[2 * W + (threadIdx.x - W)] = v;       // Gram entry
-        }
-      }
-      // ---- slice-wide barrier: two-level merge of the chunk records ----
-      // chunks arrive in groups of kGroup; the last of a group merges the group, the last
-      // group of the slice merges the group records and publishes the coefficients
-      __threadfence();
-      epi_sync();
-      const int ngs = (nchunks + kGroup - 1) / kGroup;
-      const int grp = k / kGroup;
-      const int gsize = min(kGroup, nchunks - grp * kGroup);
-      float* stage = reinterpret_cast<float*>(sm + S::kOffStage);
-      float* merged = stage + kGroup * S::kRec;   // sM scratch then the slice record
-      if (threadIdx.x == 0) {
-        ctl[0] = 0;
-        if (!ok) {
-          ctl[1] = 1;
-        } else {
-          const int prev = atomicAdd(&A.garrive[(long long)slice * A.ngroups + grp], 1);
-          ctl[0] = (prev == gsize - 1) ? 1 : 0;
-        }
-      }
-      epi_sync();
-      if (ctl[0]) {
-        __threadfence();
-        float* grec = A.grec + ((long long)slice * A.ngroups + grp) * A.stride;
-        merge_records<W>(A.partial + ((long long)slice * A.maxc + grp * kGroup) * A.stride,
-                         gsize, A.stride, grec, stage, H, cl2);
-        __threadfence();
-        epi_sync();
-        if (threadIdx.x == 0) {
-          const int prev = atomicAdd(&A.arrive[slice], 1);
-          ctl[0] = (prev == ngs - 1) ? 2 : 0;
-        }
-        epi_sync();
-      }
-      float* fin = A.fin + (long long)slice * (3 * W + kMaxWalk);
-      if (ctl[0] == 2) {
-        __threadfence();
-        float* rec = merged + 64;               // after the sM scratch (W <= 64)
-        merge_records<W>(A.grec + (long long)slice * A.ngroups * A.stride, ngs, A.stride, rec,
-                         stage, H, cl2);
-        if (threadIdx.x == 0) {
-          // Eq. (4) in rank-1 form on <P_p, P_q> = Gram / (Z_p Z_q)
-          float gam[kMaxWalk], gsum = 0.f;
-          for (int t = 0; t < H; ++t) {
-            float g = 1.f;
-            for (int u = 0; u < t; ++u) {
-              const int wp = W - H + u, wq = W - H + t;
-              g += gam[u] * rec[2 * W + pair_index(u, t)] / (rec[W + wp] * rec[W + wq]);
-            }
-            gam[t] = g;
-            gsum += g;
-          }
-          // ||C||_1 = sum_t gamma_t since every row P sums to one
-          for (int t = 0; t < kMaxWalk; ++t)
-            fin[3 * W + t] = (t < H) ? gam[t] / (gsum * rec[W + (W - H + t)]) : 0.f;
-        }
-        if (threadIdx.x < W) {
-          const int w = threadIdx.x;
-          fin[w] = rec[w];                                     // raw max
-          fin[W + w] = rec[W + w];                             // normaliser
-          fin[2 * W + w] = 1.0f / ((float)W * rec[W + w]);
-        }
-        __threadfence();
-        epi_sync();
-        if (threadIdx.x == 0) st_release(&A.ready[slice], 1);
-      } else {
-        if (threadIdx.x == 0 && !ctl[1])
-          if (!wait_at_least(&A.ready[slice], 1, A.dev_status)) ctl[1] = 1;
-        epi_sync();
-      }
-      ok = ok && !ctl[1];
-      // ---- per-chunk coefficients: fold the chunk-max shift into the final weights ----
-      if (ok && threadIdx.x < W) {
-        const int w = threadIdx.x;
-        const float shift = exp2f((s_mc[w] - __ldcg(&fin[w])) * cl2);
-        s_ca[w] = __ldcg(&fin[2 * W + w]) * shift;
-        if (w >= W - H) s_cc[w - (W - H)] = __ldcg(&fin[3 * W + (w - (W - H))]) * shift;
-      }
-      if (ok && k == 0 && (A.out.flags & kEmitStats) && threadIdx.x < W) {
-        const int w = threadIdx.x;
-        A.out.row_stats[((long long)slice * W + w) * 2] = __ldcg(&fin[w]) * rsqrtf((float)D);
-        A.out.row_stats[((long long)slice * W + w) * 2 + 1] = __ldcg(&fin[W + w]);
-      }
-      epi_sync();
-      // pass 2: a, c~, w and the order key of every row
-      const uint32_t head_id = (uint32_t)((p.layer_id_base + l) * c.kv_heads + h);
-      const uint32_t seq_id = (uint32_t)(p.seq_id_base + s);
-      for (int t = 0; t < ntiles && ok; ++t) {
-        const int j = j0 + t * kTileRows + warp * 32 + lane;
-        float a = 0.f, ct = 0.f;
-#pragma unroll
-        for (int cb = 0; cb < W; cb += 16) {
-          float v[16];
-          tmem_ld16(lane_base + t * W + cb, v);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            a = fmaf(v[i], s_ca[cb + i], a);
-            if (cb + i >= W - H) ct = fmaf(v[i], s_cc[cb + i - (W - H)], ct);
-          }
-        }
-        if (j < T) {
-          const float sj = a + p.lambda * ct;
-          const float ramp = (T > 1) ? (float)j / (float)(T - 1) : 0.f;
-          const float wj = sj + p.eps_tie * ramp;
-          const long long o = (long long)slice * c.capacity + j;
-          if (A.out.flags & kEmitA) A.out.a[o] = a;
-          if (A.out.flags & kEmitC) A.out.ctilde[o] = ct;
-          if (A.out.flags & kEmitW) A.out.w[o] = wj;
-          if (A.out.flags & kEmitKeys) {
-            uint32_t key = kForcedKey;
-            if (!(j < p.n_sink || j >= T - p.n_recent))
-              key = candidate_key(wj, c.pos[row_of(c, l, s, h, j)], p, head_id, seq_id);
-            A.out.keys[o] = key;
-          }
-        }
-      }
-      if (!ok && threadIdx.x == 0) ctl[1] = 1;
     }
-    // ---- end of chunk: TMEM reads done before the next chunk's MMAs overwrite it ----
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    it += ntiles;
-    ++chunks_done;
-    if (new_q) ++q_loads;
+  } else {
+    // =================== epilogue: warps 0-7 ===================
+    Epi<W, D> epi(A, sm, tmem, buf_cols, cl2, A.p.walk_len);
+    switch (A.p.walk_len) {
+      case 3: epi.template run<3>(bar_tfull, bar_tempty, chunk_rows, nbuf); break;
+      case 5: epi.template run<5>(bar_tfull, bar_tempty, chunk_rows, nbuf); break;
+      default: epi.template run<-1>(bar_tfull, bar_tempty, chunk_rows, nbuf); break;
+    }
   }
 
+  tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(A.tmem_cols));
@@ -630,6 +917,9 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
+long long* g_trace = nullptr;     // installed by nexus_debug_set_trace
+thread_local int32_t g_last_cfg[8];
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static bool tried = false;
@@ -651,13 +941,14 @@ cudaError_t launch_t(const nx_cache& c, const nx_params& p, const void* q, const
                      int* launches, bool* used) {
   using S = Smem<W, D>;
   *used = false;
+  for (int i = 0; i < 8; ++i) g_last_cfg[i] = 0;
   auto fn = encode_fn();
-  if (!fn) return cudaSuccess;
+  if (!fn) { g_last_cfg[0] = -1; return cudaSuccess; }
   // the whole K tensor as rows of head_dim bf16 elements; boxes of 64 columns
   const long long rows = c.page_size
                              ? (long long)c.layers * c.num_pages * c.kv_heads * c.page_size
                              : (long long)c.layers * c.seqs * c.kv_heads * c.capacity;
-  if (rows >= (1LL << 31)) return cudaSuccess;
+  if (rows >= (1LL << 31)) { g_last_cfg[0] = -2; return cudaSuccess; }
   CUtensorMap map;
   cuuint64_t gdim[2] = {(cuuint64_t)D, (cuuint64_t)rows};
   cuuint64_t gstride[1] = {(cuuint64_t)D * 2};
@@ -665,10 +956,12 @@ cudaError_t launch_t(const nx_cache& c, const nx_params& p, const void* q, const
   cuuint32_t estr[2] = {1, 1};
   if (fn(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c.k, gdim, gstride, box, estr,
          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+    g_last_cfg[0] = -3;
     return cudaSuccess;
+  }
 
-  int dev = 0, sms = 0, per_sm = 0;
+  int dev = 0, sms = 0, per_sm_api = 0;
   cudaGetDevice(&dev);
   static bool attr_set[64] = {};
   if (dev < 0 || dev >= 64) return cudaSuccess;
@@ -683,64 +976,104 @@ cudaError_t launch_t(const nx_cache& c, const nx_params& p, const void* q, const
     attr_set[dev] = true;
   }
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, score_tc_kernel<W, D>, kThreads, S::kAlloc);
-  if (per_sm < 1) return cudaSuccess;
-  if (per_sm > 2) per_sm = 2;                 // TMEM: 512 columns per SM, split evenly
-  const uint32_t tmem_cols = per_sm == 2 ? 256u : 512u;
-  const long long grid_max = (long long)sms * per_sm;
-
-  // chunk size: as many tiles as TMEM holds, but enough chunks to fill the grid
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_api, score_tc_kernel<W, D>, kThreads,
+                                                S::kAlloc);
   const long long slices = L.slices;
-  const int max_tiles = (int)(tmem_cols / W);
   const long long cap_tiles = (c.capacity + kTileRows - 1) / kTileRows;
-  // the smallest power-of-two chunk that still fits every chunk in one round of the grid
-  int tpc = max_tiles;
-  while (tpc > 1 && slices * ((cap_tiles + tpc / 2 - 1) / (tpc / 2)) <= grid_max) tpc >>= 1;
-  const int maxc = (int)((cap_tiles + tpc - 1) / tpc);
-  if (maxc > grid_max) return cudaSuccess;    // the slice barrier needs co-resident chunks
-  if (maxc > kGroup * kGroup) return cudaSuccess;   // two merge levels of 16
-  if ((long long)maxc * (long long)((c.capacity + 127) / 128) > (1LL << 40)) return cudaSuccess;
 
-  Args a;
-  a.c = c;
-  a.p = p;
-  (void)q;
-  a.qimg = reinterpret_cast<const unsigned char*>(ws + L.qbar);
-  a.tmem_cols = tmem_cols;
-  a.partial = reinterpret_cast<float*>(ws + L.stats);
-  a.fin = reinterpret_cast<float*>(ws + L.fin);
-  a.arrive = reinterpret_cast<int*>(ws + L.barriers);
-  a.ready = a.arrive + slices;
-  a.garrive = reinterpret_cast<int*>(ws + L.group_arrive);
-  a.grec = reinterpret_cast<float*>(ws + L.group_rec);
-  a.ngroups = L.groups_per_slice;
-  a.newlen = reinterpret_cast<const int32_t*>(ws + L.newlen);
-  a.out = out;
-  a.dev_status = dev_status;
-  a.tiles_per_chunk = tpc;
-  a.maxc = maxc;
-  a.stride = L.stats_stride;
-  a.total_ids = slices * maxc;
-  long long grid = a.total_ids < grid_max ? a.total_ids : grid_max;
+  // One CTA per SM with all 512 TMEM columns (its 8 epilogue warps hide latency).
+  for (int per_sm = 1; per_sm >= 1; --per_sm) {
+    const uint32_t tmem_cols = 512u;
+    const long long grid_max = (long long)sms * per_sm;
+    // Chunk size and grid: every slice's chunks must be co-resident (the slice barrier),
+    // and a round of the grid should hold whole slices (a slice split across two rounds
+    // makes its first chunks wait a whole round). Among chunk sizes up to what a TMEM
+    // buffer holds (and 16 tiles), pick the fewest rounds x chunk tiles; prefer two
+    // buffers (the next chunk's MMAs overlap this chunk's epilogue).
+    int nbuf = 0, tpc = 0, maxc = 0;
+    long long grid_sel = 0, best = -1;
+    for (int nb = 2; nb >= 1; --nb) {
+      const int max_tiles = min(16, (int)(tmem_cols / nb / W));
+      for (int t = 1; t <= max_tiles; ++t) {
+        const int mc = (int)((cap_tiles + t - 1) / t);
+        if (mc > grid_max || mc > kGroup * kGroup) continue;
+        const long long per = grid_max / mc;                 // whole slices per round
+        const long long rounds = (slices + per - 1) / per;
+        // a single buffer overlaps less; ties go to fewer rounds (fewer barrier waits)
+        long long cost = (rounds * t * (nb == 2 ? 2 : 3)) * 4096 + rounds;
+        if (best < 0 || cost < best) {
+          best = cost;
+          nbuf = nb;
+          tpc = t;
+          maxc = mc;
+          grid_sel = per * mc;
+        }
+      }
+    }
+    if (!nbuf) { g_last_cfg[0] = -4; continue; }
+    Args a;
+    a.c = c;
+    a.p = p;
+    (void)q;
+    a.qimg = reinterpret_cast<const unsigned char*>(ws + L.qbar);
+    a.tmem_cols = tmem_cols;
+    a.partial = reinterpret_cast<float*>(ws + L.stats);
+    a.fin = reinterpret_cast<float*>(ws + L.fin);
+    a.arrive = reinterpret_cast<int*>(ws + L.barriers);
+    a.ready = a.arrive + slices;
+    a.garrive = reinterpret_cast<int*>(ws + L.group_arrive);
+    a.grec = reinterpret_cast<float*>(ws + L.group_rec);
+    a.ngroups = L.groups_per_slice;
+    a.newlen = reinterpret_cast<const int32_t*>(ws + L.newlen);
+    a.out = out;
+    a.dev_status = dev_status;
+    a.tiles_per_chunk = tpc;
+    a.nbuf = nbuf;
+    a.maxc = maxc;
+    a.stride = L.stats_stride;
+    a.total_ids = slices * maxc;
+    a.trace = g_trace;
+    const long long grid = a.total_ids < grid_sel ? a.total_ids : grid_sel;
 
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = S::kAlloc;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, score_tc_kernel<W, D>, map, a);
-  if (e != cudaSuccess) return e;
-  note_launch(st, launches, "score_tc");
-  *used = true;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = S::kAlloc;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, score_tc_kernel<W, D>, map, a);
+    if (e == cudaErrorCooperativeLaunchTooLarge) {
+      (void)cudaGetLastError();
+      g_last_cfg[0] = -5;
+      g_last_cfg[1] = per_sm_api;
+      continue;
+    }
+    if (e != cudaSuccess) return e;
+    g_last_cfg[0] = per_sm;
+    g_last_cfg[1] = per_sm_api;
+    g_last_cfg[2] = (int32_t)grid;
+    g_last_cfg[3] = tpc;
+    g_last_cfg[4] = nbuf;
+    g_last_cfg[5] = maxc;
+    g_last_cfg[6] = (int32_t)tmem_cols;
+    g_last_cfg[7] = S::kAlloc;
+    note_launch(st, launches, "score_tc");
+    *used = true;
+    return cudaSuccess;
+  }
   return cudaSuccess;
 }
 
 }  // namespace tc
+
+void tc_set_trace(long long* buf) { tc::g_trace = buf; }
+void tc_last_config(int32_t* out) {
+  for (int i = 0; i < 8; ++i) out[i] = tc::g_last_cfg[i];
+}
 
 bool tc_supported(const nx_cache& c, const nx_params& p) {
   if (c.dtype != NX_DTYPE_BF16) return false;

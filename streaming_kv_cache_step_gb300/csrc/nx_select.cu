@@ -4,8 +4,8 @@
 // slots, else the monotone image of kappa_j = ln(u_j)/w_j (reservoir) or w_j (top-K).
 // Keeping the B largest composite keys (key, slot) keeps the forced slots plus the K
 // largest kappa, ties to the newer slot. One thread block per slice finds the B-th
-// largest composite by an MSB-first radix select (three 11/11/10-bit digit passes on the
-// key, three more on the slot only when the threshold key is tied), then writes the kept
+// largest composite by an MSB-first radix select (four 8-bit digit passes on the key,
+// four more on the slot only when the threshold key is tied), then writes the kept
 // slots in ascending order with a block-wide ballot scan.
 #include "nx_internal.cuh"
 
@@ -33,7 +33,7 @@ __global__ void keys_from_w_kernel(nx_cache c, nx_params p, const float* __restr
   keys[o] = key;
 }
 
-constexpr int kDigitBits = 11;                  // three passes cover 32 bits
+constexpr int kDigitBits = 8;                   // four passes cover 32 bits
 constexpr int kBins = 1 << kDigitBits;
 constexpr int kBinsPerLane = kBins / 32;
 
@@ -120,10 +120,9 @@ select_kernel(nx_cache c, const uint32_t* __restrict__ keys, int32_t* __restrict
   uint32_t prefix = 0, pmask = 0;
   int need = B;
   int eq_count = 0;
-  // digits: bits 21..31, 10..20, 0..9 (the last digit has 10 bits; its upper bin is empty)
-  for (int pass = 0; pass < 3; ++pass) {
-    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-    const uint32_t dmask = pass == 2 ? 0x3FFu : 0x7FFu;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    const uint32_t dmask = 0xFFu;
     for (int i = threadIdx.x; i < kBins; i += blockDim.x) hist[i] = 0;
     __syncthreads();
     digit_hist<SMEM>(kk, T, pmask, prefix, shift, false, 0, hist);
@@ -142,9 +141,9 @@ select_kernel(nx_cache c, const uint32_t* __restrict__ keys, int32_t* __restrict
   if (eq_count > need) {
     uint32_t sp = 0, sm = 0;
     int sneed = need;
-    for (int pass = 0; pass < 3; ++pass) {
-      const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-      const uint32_t dmask = pass == 2 ? 0x3FFu : 0x7FFu;
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+      const uint32_t dmask = 0xFFu;
       for (int i = threadIdx.x; i < kBins; i += blockDim.x) hist[i] = 0;
       __syncthreads();
       digit_hist<SMEM>(kk, T, sm, sp, shift, true, tau, hist);
@@ -158,7 +157,7 @@ select_kernel(nx_cache c, const uint32_t* __restrict__ keys, int32_t* __restrict
     }
     slot_tau = (int)sp;
   }
-  // ---- write kept slots, ascending ----
+  // ---- write kept slots, ascending: ballot per warp, shuffle scan of the warp counts ----
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   int base = 0;
   for (int j0 = 0; j0 < T; j0 += blockDim.x) {
@@ -171,14 +170,16 @@ select_kernel(nx_cache c, const uint32_t* __restrict__ keys, int32_t* __restrict
     const unsigned bal = __ballot_sync(0xffffffffu, take);
     if (lane == 0) wcount[warp] = __popc(bal);
     __syncthreads();
-    int off = base;
-    int tot = 0;
-    for (int w = 0; w < nw; ++w) {
-      const int cw = wcount[w];
-      if (w < warp) off += cw;
-      tot += cw;
+    int cw = lane < nw ? wcount[lane] : 0;          // every warp scans the warp counts
+    int incl = cw;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
     }
-    if (take) out[off + __popc(bal & ((1u << lane) - 1u))] = j;
+    const int excl_w = __shfl_sync(0xffffffffu, incl - cw, warp);
+    const int tot = __shfl_sync(0xffffffffu, incl, 31);
+    if (take) out[base + excl_w + __popc(bal & ((1u << lane) - 1u))] = j;
     base += tot;
     __syncthreads();
   }

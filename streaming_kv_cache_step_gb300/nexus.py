@@ -27,7 +27,8 @@ MODE_RESERVOIR, MODE_TOPK = 0, 1
 SYMBOLS = ("nexus_workspace_bytes", "nexus_direct_scores", "nexus_walk",
            "nexus_reservoir_select", "kv_compact", "nexus_evict_step", "nx_status_string",
            "nexus_last_launch_count", "nexus_debug_compact", "nexus_last_launch_name",
-           "nexus_profile_next_call", "nexus_debug_force_simt")
+           "nexus_profile_next_call", "nexus_debug_force_simt", "nexus_debug_set_trace",
+           "nexus_debug_scorer_config")
 
 
 class NexusError(RuntimeError):
@@ -88,6 +89,10 @@ def load(path: str = LIB_PATH):
             lib.nexus_profile_next_call.restype = None
             lib.nexus_debug_force_simt.argtypes = [ctypes.c_int32]
             lib.nexus_debug_force_simt.restype = None
+            lib.nexus_debug_set_trace.argtypes = [ctypes.c_void_p]
+            lib.nexus_debug_set_trace.restype = None
+            lib.nexus_debug_scorer_config.argtypes = [ctypes.c_void_p]
+            lib.nexus_debug_scorer_config.restype = None
             _lib = lib
     return _lib
 
@@ -95,6 +100,20 @@ def load(path: str = LIB_PATH):
 def force_simt(on: bool) -> None:
     """Route scoring to the CUDA-core scorer even where the tensor-core one applies."""
     load().nexus_debug_force_simt(1 if on else 0)
+
+
+def scorer_config() -> dict:
+    """Configuration of the last tensor-core scorer launch made from this thread."""
+    out = (ctypes.c_int32 * 8)()
+    load().nexus_debug_scorer_config(out)
+    keys = ("ctas_per_sm", "occupancy_api", "grid", "tiles_per_chunk", "tmem_buffers",
+            "chunks_per_slice", "tmem_cols", "smem_bytes")
+    return dict(zip(keys, list(out)))
+
+
+def set_trace(buf) -> None:
+    """Install (int64 CUDA tensor) or remove (None) the scorer's phase-trace buffer."""
+    load().nexus_debug_set_trace(None if buf is None else ctypes.c_void_p(buf.data_ptr()))
 
 
 def status_string(status: int) -> str:

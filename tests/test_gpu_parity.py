@@ -235,9 +235,10 @@ def test_tensor_core_scorer_matches_cuda_core_scorer(name):
             nexus.walk(run.cache, run.q, run.params, w, ct, run.ws, run.status)
             run.check_status()
             names = nexus.last_launch_names()
+            cfg = nexus.scorer_config()
         finally:
             nexus.force_simt(False)
-        assert ("score_tc" in names) != simt, names
+        assert ("score_tc" in names) != simt, (names, cfg)
         outs.append((w.cpu().numpy(), ct.cpu().numpy()))
     (w_tc, c_tc), (w_si, c_si) = outs
     lens = run.lens()
