@@ -28,13 +28,13 @@
 namespace nx {
 namespace tc {
 
-constexpr int kEpiWarps = 8;           // warps 0-7: epilogue (two warpgroups)
+constexpr int kEpiWarps = 16;          // warps 0-15: epilogue (four warpgroups)
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kProducerWarp = kEpiWarps;       // TMA producer
 constexpr int kMmaWarp = kEpiWarps + 1;        // MMA issuer, TMEM owner
 constexpr int kThreads = kEpiThreads + 64;
 constexpr int kTileRows = 128;
-constexpr int kStages = 4;
+constexpr int kMaxChunkTiles = 8;      // tiles per chunk (the pass-2 partials are sized for it)
 constexpr long long kWaitLimit = 1LL << 22;   // mbarrier polls before giving up
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -46,12 +46,7 @@ struct Args {
   int nbuf;                // TMEM buffers (2: the next chunk's MMAs overlap this epilogue)
   long long* trace;        // optional phase trace: [grid][kTraceEvents][2] (null: off)
   float* partial;          // [slices][maxc][stride]
-  float* fin;              // [slices][3W + kMaxWalk]
-  int* arrive;             // [slices] groups of the slice merged
-  int* ready;              // [slices] final coefficients published
-  int* garrive;            // [slices][ngroups] chunks of each group published
-  float* grec;             // [slices][ngroups][stride] merged group records
-  int ngroups;             // group records per slice (chunks are merged 16 at a time)
+  int* arrive;             // [slices] chunks whose records are published
   const int32_t* newlen;   // [slices]
   ScoreOut out;
   int32_t* dev_status;
@@ -211,6 +206,47 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
       : "memory");
 }
 
+// N (4, 8 or 16) consecutive TMEM columns of this thread's lane, loaded and awaited.
+template <int N>
+__device__ __forceinline__ void tmem_ldn(uint32_t taddr, float* v) {
+  uint32_t r[N];
+  if constexpr (N == 4) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr));
+  } else if constexpr (N == 8) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+  } else {
+    tmem_ld16_nowait(taddr, r);
+  }
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < N; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_stn(uint32_t taddr, const float* v) {
+  uint32_t r[N];
+#pragma unroll
+  for (int i = 0; i < N; ++i) r[i] = __float_as_uint(v[i]);
+  if constexpr (N == 4) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
+                 : "memory");
+  } else if constexpr (N == 8) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(
+                     taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+                 "r"(r[7])
+                 : "memory");
+  } else {
+    tmem_st16(taddr, v);
+  }
+}
+
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -243,7 +279,8 @@ __device__ __forceinline__ float warp_sum(float x) {
 // ---------------------------------------------------------------------------
 // Merging chunk statistics
 // ---------------------------------------------------------------------------
-constexpr int kGroup = 64;    // records merged at a time
+constexpr int kGroup = 64;        // records merged at a time
+constexpr int kMaxBatches = 4;    // chunks per slice <= kGroup * kMaxBatches
 
 // A record holds, for the rows it covers: per window row w the maximum raw logit m_w and
 // sum_j exp((l_wj - m_w)/sqrt(d)) (natural-log units), and per walk-row pair (p, q) the
@@ -251,7 +288,7 @@ constexpr int kGroup = 64;    // records merged at a time
 // n <= kGroup records (global memory, `stride` floats apart) into one record `dst` of the same
 // form, with the epilogue threads: every value is loaded into shared memory at once
 // (independent loads, one round trip), then combined in a fixed order.
-template <int W>
+template <int W, bool GSRC>
 __device__ __forceinline__ void merge_records(const float* src, int n, int stride, float* dst,
                                               float* stage, int H, float cl2) {
   constexpr int R = 2 * W + kMaxPairs;
@@ -259,10 +296,10 @@ __device__ __forceinline__ void merge_records(const float* src, int n, int strid
   const int tid = threadIdx.x;
   for (int idx = tid; idx < n * R; idx += kEpiThreads) {
     const int i = idx / R, f = idx - i * R;
-    stage[idx] = __ldcg(&src[(long long)i * stride + f]);
+    stage[idx] = GSRC ? __ldcg(&src[(long long)i * stride + f]) : src[i * stride + f];
   }
   float* sM = stage + kGroup * R;      // merged maxima (W <= 64 floats)
-  float* part = sM + 64 + R;           // [PARTS][W] partial results (after the dst slot)
+  float* part = sM + 64;               // [PARTS][W] then [GP][kMaxPairs] partial results
   epi_sync();
   const int w = tid % W, pt = tid / W;
   float m = -INFINITY;
@@ -279,11 +316,10 @@ __device__ __forceinline__ void merge_records(const float* src, int n, int strid
   float z = 0.f;
   for (int i = pt; i < n; i += PARTS) z += stage[i * R + W + w] * exp2f((stage[i * R + w] - Mw) * cl2);
   part[pt * W + w] = z;
-  // Gram pairs: threads split over (pair, part of the records)
   constexpr int GP = kEpiThreads / kMaxPairs;  // 9 parts for 28 pairs
   float g = 0.f;
-  int pu = 0, pt2 = 0, gi = tid % kMaxPairs;
-  const int gpart = tid / kMaxPairs;
+  int pu = 0, pt2 = 0;
+  const int gi = tid % kMaxPairs, gpart = tid / kMaxPairs;
   pair_of(gi, pu, pt2);
   if (gpart < GP && pt2 < H) {
     const int wp = W - H + pu, wq = W - H + pt2;
@@ -293,7 +329,7 @@ __device__ __forceinline__ void merge_records(const float* src, int n, int strid
       g += r[2 * W + gi] * exp2f(((r[wp] - mp) + (r[wq] - mq)) * cl2);
     }
   }
-  float* gpartial = part + PARTS * W;          // [GP][kMaxPairs]
+  float* gpartial = part + PARTS * W;
   if (gpart < GP) gpartial[gpart * kMaxPairs + gi] = g;
   epi_sync();
   if (tid < W) {
@@ -310,11 +346,18 @@ __device__ __forceinline__ void merge_records(const float* src, int n, int strid
   epi_sync();
 }
 
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
 template <int W, int D>
 struct Smem {
+  static constexpr int kStages = (W == 64) ? 3 : 4;       // K tiles in flight
   static constexpr int KB = D / 64;                       // 128-byte column blocks per row
   static constexpr int kRegionA = kTileRows * 128;        // one column block of a K tile
   static constexpr int kTileBytes = KB * kRegionA;
@@ -327,13 +370,17 @@ struct Smem {
   static constexpr int kOffBar = kOffQ + kQBytes;         // 16 mbarriers
   static constexpr int kOffMisc = kOffBar + 128;          // tmem slot + control words
   static constexpr int kOffRed = kOffMisc + 64;           // [kEpiWarps][kRedStride]
-  static constexpr int kOffMc = kOffRed + kEpiWarps * kRedStride * 4;   // [2][W] chunk maxima
-  static constexpr int kOffCa = kOffMc + 2 * W * 4;       // [W] a coefficients
+  static constexpr int kOffMc = kOffRed + kEpiWarps * kRedStride * 4;   // [3][W] chunk maxima
+  static constexpr int kOffCa = kOffMc + 3 * W * 4;       // [W] a coefficients
   static constexpr int kOffCc = kOffCa + W * 4;           // [kMaxWalk] walk coefficients
-  // merge staging: [kGroup][kRec] records, 64 maxima, one merged record, partial sums
-  static constexpr int kOffStage = kOffCc + kMaxWalk * 4;
-  static constexpr int kBytes =
-      kOffStage + (kGroup * kRec + 64 + kRec + kEpiThreads + kEpiThreads) * 4;
+  static constexpr int kOffNm = kOffCc + kMaxWalk * 4;    // [W] -max * cl2 of the chunk
+  static constexpr int kOffRec = kOffNm + W * 4;          // [kMaxBatches + 1][kRec] merged
+  static constexpr int kOffPart = kOffRec + (kMaxBatches + 1) * kRec * 4;
+  // pass-2 partial a per tile, warpgroup and row; the walk term per tile and row
+  static constexpr int kOffCt = kOffPart + kMaxChunkTiles * 4 * kTileRows * 4;
+  // merge staging: [kGroup][kRec] records, 64 maxima, partial sums
+  static constexpr int kOffStage = kOffCt + kMaxChunkTiles * kTileRows * 4;
+  static constexpr int kBytes = kOffStage + (kGroup * kRec + 64 + kEpiThreads + kEpiThreads) * 4;
   static constexpr int kAlloc = kBytes + 1024;            // slack for 1024-byte alignment
 };
 
@@ -396,22 +443,28 @@ __device__ __forceinline__ Chunk decode_chunk(const Args& A, long long id, int c
   return ch;
 }
 
-// Epilogue state shared by the passes.
+// Epilogue state shared by the passes. The W query columns are split over the four
+// warpgroups (warpgroup g owns columns [g W/4, (g+1) W/4)); the four warps of a warpgroup
+// own the 128 rows of a tile (TMEM lanes). The walk rows, the last H <= W/4 columns,
+// belong to warpgroup 3.
 template <int W, int D>
 struct Epi {
+  static constexpr int CW = W / 4;
   const Args& A;
   uint8_t* sm;
   uint32_t tmem;
   uint32_t buf_cols;
   float cl2;
   int H;
-  int warp, lane, wg;   // wg: warpgroup, which takes every other tile of a chunk
+  int warp, lane, wg, lg, col0;
   int nev = 0;          // trace events written (thread 0)
   __device__ Epi(const Args& a, uint8_t* s, uint32_t t, uint32_t bc, float c2, int h)
       : A(a), sm(s), tmem(t), buf_cols(bc), cl2(c2), H(h) {
     warp = threadIdx.x >> 5;
     lane = threadIdx.x & 31;
     wg = warp >> 2;
+    lg = warp & 3;
+    col0 = wg * CW;
   }
   __device__ float* red() { return reinterpret_cast<float*>(sm + Smem<W, D>::kOffRed); }
   __device__ float* mc(uint32_t b) {
@@ -419,20 +472,15 @@ struct Epi {
   }
   __device__ float* ca() { return reinterpret_cast<float*>(sm + Smem<W, D>::kOffCa); }
   __device__ float* cc() { return reinterpret_cast<float*>(sm + Smem<W, D>::kOffCc); }
-  __device__ uint32_t lane_base(const Chunk& ch) {
-    return tmem + ((uint32_t)((warp & 3) * 32) << 16) + ch.b * buf_cols;
+  __device__ float* nm() { return reinterpret_cast<float*>(sm + Smem<W, D>::kOffNm); }
+  __device__ float* recs() { return reinterpret_cast<float*>(sm + Smem<W, D>::kOffRec); }
+  __device__ float* apart() { return reinterpret_cast<float*>(sm + Smem<W, D>::kOffPart); }
+  __device__ float* ctp() { return reinterpret_cast<float*>(sm + Smem<W, D>::kOffCt); }
+  __device__ uint32_t taddr(const Chunk& ch, int t) {
+    return tmem + ((uint32_t)(lg * 32) << 16) + ch.b * buf_cols + (uint32_t)(t * W + col0);
   }
   __device__ bool row_valid(const Chunk& ch, int t) {
-    return ch.j0 + t * kTileRows + (warp & 3) * 32 + lane < ch.T;
-  }
-
-  // Combine per-warp partials red[warp][i], i < n, over the epilogue warps.
-  __device__ float combine(int i, bool is_max) {
-    constexpr int RS = Smem<W, D>::kRedStride;
-    float v = red()[i];
-    for (int w8 = 1; w8 < kEpiWarps; ++w8)
-      v = is_max ? fmaxf(v, red()[w8 * RS + i]) : v + red()[w8 * RS + i];
-    return v;
+    return ch.j0 + t * kTileRows + lg * 32 + lane < ch.T;
   }
 
   // Passes 1a/1b: chunk maxima, e = exp((l - max)/sqrt(d)) written back to TMEM, chunk
@@ -440,268 +488,262 @@ struct Epi {
   template <int HT>
   __device__ void stats(const Chunk& ch) {
     constexpr int RS = Smem<W, D>::kRedStride;
-    constexpr int NB = (W >= 32) ? 32 : 16;
-    const uint32_t lb = lane_base(ch);
     float* m = mc(ch.b);
-    float mx[W];
+    float mx[CW];
 #pragma unroll
-    for (int w = 0; w < W; ++w) mx[w] = -INFINITY;
-    for (int t = wg; t < ch.ntiles; t += 2) {
+    for (int i = 0; i < CW; ++i) mx[i] = -INFINITY;
+    for (int t = 0; t < ch.ntiles; ++t) {
       const bool valid = row_valid(ch, t);
+      float v[CW];
+      tmem_ldn<CW>(taddr(ch, t), v);
 #pragma unroll
-      for (int cb = 0; cb < W; cb += NB) {
-        float v[NB];
-        tmem_load<NB>(lb + t * W + cb, v);
-#pragma unroll
-        for (int i = 0; i < NB; ++i) mx[cb + i] = fmaxf(mx[cb + i], valid ? v[i] : -INFINITY);
-      }
+      for (int i = 0; i < CW; ++i) mx[i] = fmaxf(mx[i], valid ? v[i] : -INFINITY);
     }
     if (threadIdx.x == 0) trace_ev(A, nev, 10);
 #pragma unroll
-    for (int w = 0; w < W; ++w) {
-      const float x = warp_max_redux(mx[w]);
-      if (lane == 0) red()[warp * RS + w] = x;
+    for (int i = 0; i < CW; ++i) {
+      const float x = warp_max_redux(mx[i]);
+      if (lane == 0) red()[warp * RS + col0 + i] = x;
     }
     epi_sync();
-    if (threadIdx.x < W) m[threadIdx.x] = combine(threadIdx.x, true);
+    if (threadIdx.x < W) {
+      const int col = threadIdx.x, g = col / CW;
+      float x = red()[(4 * g) * RS + col];
+      for (int q = 1; q < 4; ++q) x = fmaxf(x, red()[(4 * g + q) * RS + col]);
+      m[col] = x;
+      nm()[col] = -x * cl2;
+    }
     epi_sync();
     if (threadIdx.x == 0) trace_ev(A, nev, 11);
-    float z[W], gp[kMaxPairs];
+    float z[CW], gp[kMaxPairs], snm[CW];
 #pragma unroll
-    for (int w = 0; w < W; ++w) z[w] = 0.f;
+    for (int i = 0; i < CW; ++i) {
+      z[i] = 0.f;
+      snm[i] = nm()[col0 + i];
+    }
 #pragma unroll
     for (int i = 0; i < kMaxPairs; ++i) gp[i] = 0.f;
-    for (int t = wg; t < ch.ntiles; t += 2) {
+    const bool walk_wg = (wg == 3);
+    for (int t = 0; t < ch.ntiles; ++t) {
       const bool valid = row_valid(ch, t);
-      float ew[kMaxWalk];
+      float v[CW];
+      const uint32_t ta = taddr(ch, t);
+      tmem_ldn<CW>(ta, v);
 #pragma unroll
-      for (int cb = 0; cb < W; cb += NB) {
-        float v[NB];
-        tmem_load<NB>(lb + t * W + cb, v);
-#pragma unroll
-        for (int i = 0; i < NB; ++i) {
-          const float e = valid ? exp2f((v[i] - m[cb + i]) * cl2) : 0.f;
-          v[i] = e;
-          z[cb + i] += e;
-        }
-        tmem_st16(lb + t * W + cb, v);
-        if (NB == 32) tmem_st16(lb + t * W + cb + 16, v + 16);
-        if (cb + NB == W) {   // the walk rows W-H .. W-1 are the last H columns
-          if (HT >= 0) {
-#pragma unroll
-            for (int tt = 0; tt < kMaxWalk; ++tt) ew[tt] = (tt < HT) ? v[NB - HT + tt] : 0.f;
-          } else {
-#pragma unroll
-            for (int tt = 0; tt < kMaxWalk; ++tt) {
-              float x = 0.f;
-#pragma unroll
-              for (int i = NB - kMaxWalk; i < NB; ++i)
-                if (tt < H && i == NB - H + tt) x = v[i];
-              ew[tt] = x;
-            }
-          }
-        }
+      for (int i = 0; i < CW; ++i) {
+        const float e = valid ? ex2_approx(fmaf(v[i], cl2, snm[i])) : 0.f;
+        v[i] = e;
+        z[i] += e;
       }
-      if (HT >= 0) {
+      tmem_stn<CW>(ta, v);
+      if (walk_wg) {
+        float ew[kMaxWalk];
+        if (HT >= 0) {
 #pragma unroll
-        for (int tt = 1; tt < (HT > 0 ? HT : 1); ++tt)
+          for (int tt = 0; tt < kMaxWalk; ++tt) ew[tt] = (tt < HT) ? v[CW - HT + tt] : 0.f;
 #pragma unroll
-          for (int uu = 0; uu < tt; ++uu) gp[pair_index(uu, tt)] += ew[uu] * ew[tt];
-      } else {
+          for (int tt = 1; tt < (HT > 0 ? HT : 1); ++tt)
 #pragma unroll
-        for (int tt = 1; tt < kMaxWalk; ++tt)
+            for (int uu = 0; uu < tt; ++uu) gp[pair_index(uu, tt)] += ew[uu] * ew[tt];
+        } else {
 #pragma unroll
-          for (int uu = 0; uu < tt; ++uu) gp[pair_index(uu, tt)] += ew[uu] * ew[tt];
+          for (int tt = 0; tt < kMaxWalk; ++tt) {
+            float x = 0.f;
+#pragma unroll
+            for (int i = 0; i < CW; ++i)
+              if (tt < H && i == CW - H + tt) x = v[i];
+            ew[tt] = x;
+          }
+#pragma unroll
+          for (int tt = 1; tt < kMaxWalk; ++tt)
+#pragma unroll
+            for (int uu = 0; uu < tt; ++uu) gp[pair_index(uu, tt)] += ew[uu] * ew[tt];
+        }
       }
     }
     tmem_st_wait();
     if (threadIdx.x == 0) trace_ev(A, nev, 12);
 #pragma unroll
-    for (int w = 0; w < W; ++w) {
-      const float x = warp_sum(z[w]);
-      if (lane == 0) red()[warp * RS + w] = x;
+    for (int i = 0; i < CW; ++i) {
+      const float x = warp_sum(z[i]);
+      if (lane == 0) red()[warp * RS + col0 + i] = x;
     }
-    constexpr int NP = (HT >= 0) ? (HT * (HT - 1) / 2 > 0 ? HT * (HT - 1) / 2 : 0) : kMaxPairs;
+    if (walk_wg) {
+      constexpr int NP = (HT >= 0) ? (HT * (HT - 1) / 2 > 0 ? HT * (HT - 1) / 2 : 0) : kMaxPairs;
 #pragma unroll
-    for (int i = 0; i < kMaxPairs; ++i) {
-      const float x = (i < NP) ? warp_sum(gp[i]) : 0.f;
-      if (lane == 0) red()[warp * RS + W + i] = x;
+      for (int i = 0; i < kMaxPairs; ++i) {
+        const float x = (i < NP) ? warp_sum(gp[i]) : 0.f;
+        if (lane == 0) red()[warp * RS + W + i] = x;
+      }
     }
     epi_sync();
     float* rec = A.partial + ((long long)ch.slice * A.maxc + ch.k) * A.stride;
     if (threadIdx.x < W) {
-      rec[threadIdx.x] = m[threadIdx.x];                     // chunk max (raw)
-      rec[W + threadIdx.x] = combine(threadIdx.x, false);    // sum relative to it
+      const int col = threadIdx.x, g = col / CW;
+      float x = 0.f;
+      for (int q = 0; q < 4; ++q) x += red()[(4 * g + q) * RS + col];
+      rec[col] = m[col];                  // chunk max (raw)
+      rec[W + col] = x;                   // sum relative to it
     } else if (threadIdx.x < W + kMaxPairs) {
-      rec[W + threadIdx.x] = combine(threadIdx.x, false);    // Gram entry
+      const int k = threadIdx.x - W;
+      float x = 0.f;
+      for (int q = 0; q < 4; ++q) x += red()[(12 + q) * RS + W + k];
+      rec[2 * W + k] = x;                 // Gram entry
     }
   }
 
-  // Publish the chunk's record; the last chunk of a group merges the group, the last group
-  // of the slice merges the groups and publishes the coefficients. Never waits.
+  // Publish the chunk's record: count it in for its slice (thread 0, after a fence).
   __device__ void publish(const Chunk& ch, bool ok) {
     using S = Smem<W, D>;
     int* ctl = reinterpret_cast<int*>(sm + S::kOffMisc + 16);
-    const int ngs = (ch.nchunks + kGroup - 1) / kGroup;
-    const int grp = ch.k / kGroup;
-    const int gsize = min(kGroup, ch.nchunks - grp * kGroup);
-    float* stage = reinterpret_cast<float*>(sm + S::kOffStage);
-    float* merged = stage + kGroup * S::kRec;
-    // every epilogue thread's record stores precede the barrier; thread 0 then fences and
-    // signals (release), and fences again after a successful count (acquire)
     epi_sync();
     if (threadIdx.x == 0) {
-      ctl[0] = 0;
       if (!ok) {
         ctl[1] = 1;
       } else {
         __threadfence();
-        const int prev = atomicAdd(&A.garrive[(long long)ch.slice * A.ngroups + grp], 1);
-        ctl[0] = (prev == gsize - 1) ? 1 : 0;
-        if (ctl[0]) __threadfence();
-      }
-    }
-    epi_sync();
-    if (ctl[0] && ngs > 1) {
-      float* grec = A.grec + ((long long)ch.slice * A.ngroups + grp) * A.stride;
-      merge_records<W>(A.partial + ((long long)ch.slice * A.maxc + grp * kGroup) * A.stride,
-                       gsize, A.stride, grec, stage, H, cl2);
-      if (threadIdx.x == 0) {
-        __threadfence();
-        const int prev = atomicAdd(&A.arrive[ch.slice], 1);
-        ctl[0] = (prev == ngs - 1) ? 2 : 0;
-        if (ctl[0]) __threadfence();
-      }
-      epi_sync();
-    } else if (ctl[0]) {
-      if (threadIdx.x == 0) ctl[0] = 2;         // one group: its last chunk merges directly
-      epi_sync();
-    }
-    if (ctl[0] == 2) {
-      float* fin = A.fin + (long long)ch.slice * (3 * W + kMaxWalk);
-      float* rec = merged + 64;
-      if (ngs > 1)
-        merge_records<W>(A.grec + (long long)ch.slice * A.ngroups * A.stride, ngs, A.stride, rec,
-                         stage, H, cl2);
-      else
-        merge_records<W>(A.partial + (long long)ch.slice * A.maxc * A.stride, gsize, A.stride,
-                         rec, stage, H, cl2);
-      if (threadIdx.x == 0) {
-        // Eq. (4) in rank-1 form on <P_u, P_t> = Gram / (Z_u Z_t)
-        float gam[kMaxWalk], gsum = 0.f;
-        for (int t = 0; t < H; ++t) {
-          float g = 1.f;
-          for (int u = 0; u < t; ++u)
-            g += gam[u] * rec[2 * W + pair_index(u, t)] /
-                 (rec[W + (W - H + u)] * rec[W + (W - H + t)]);
-          gam[t] = g;
-          gsum += g;
-        }
-        // ||C||_1 = sum_t gamma_t since every row P sums to one
-        for (int t = 0; t < kMaxWalk; ++t)
-          fin[3 * W + t] = (t < H) ? gam[t] / (gsum * rec[W + (W - H + t)]) : 0.f;
-      }
-      if (threadIdx.x < W) {
-        const int w = threadIdx.x;
-        fin[w] = rec[w];                                      // raw max
-        fin[W + w] = rec[W + w];                              // normaliser
-        fin[2 * W + w] = 1.0f / ((float)W * rec[W + w]);
-      }
-      epi_sync();
-      if (threadIdx.x == 0) {
-        __threadfence();
-        st_release(&A.ready[ch.slice], 1);
-        trace_ev(A, nev, 7 + 1000 * (ch.slice + 1));
+        atomicAdd(&A.arrive[ch.slice], 1);
       }
     }
   }
 
-  // Wait for the slice's coefficients, then a, c~, w and the order key of every row.
+  // Once every chunk of the slice is counted in, merge all their records here (in batches
+  // of kGroup) into one: per window row the global maximum and normaliser, and the Gram.
+  __device__ float* merge_slice(const Chunk& ch) {
+    using S = Smem<W, D>;
+    float* stage = reinterpret_cast<float*>(sm + S::kOffStage);
+    float* out = recs() + kMaxBatches * S::kRec;
+    const float* base = A.partial + (long long)ch.slice * A.maxc * A.stride;
+    const int nb = (ch.nchunks + kGroup - 1) / kGroup;
+    if (nb == 1) {
+      merge_records<W, true>(base, ch.nchunks, A.stride, out, stage, H, cl2);
+    } else {
+      for (int b = 0; b < nb; ++b)
+        merge_records<W, true>(base + (long long)b * kGroup * A.stride,
+                               min(kGroup, ch.nchunks - b * kGroup), A.stride,
+                               recs() + b * S::kRec, stage, H, cl2);
+      merge_records<W, false>(recs(), nb, S::kRec, out, stage, H, cl2);
+    }
+    return out;
+  }
+
+  // Wait for the slice, merge, then a, c~, w and the order key of every row.
   template <int HT>
   __device__ bool emit(const Chunk& ch) {
     using S = Smem<W, D>;
-    constexpr int NB = (W >= 32) ? 32 : 16;
     int* ctl = reinterpret_cast<int*>(sm + S::kOffMisc + 16);
     const nx_cache& c = A.c;
     const nx_params& p = A.p;
-    // the positions of this thread's rows (needed for the keys), loaded before waiting
-    constexpr int kMaxRows = 8;
-    int32_t posv[kMaxRows];
+    // rows this thread finalizes: tiles t = wg, wg + 4 (at most two); positions first
+    int32_t posv[2];
 #pragma unroll
-    for (int r = 0; r < kMaxRows; ++r) {
-      const int t = wg + 2 * r;
-      const int j = ch.j0 + t * kTileRows + (warp & 3) * 32 + lane;
+    for (int r = 0; r < 2; ++r) {
+      const int t = wg + 4 * r;
+      const int j = ch.j0 + t * kTileRows + lg * 32 + lane;
       posv[r] = (t < ch.ntiles && j < ch.T && (A.out.flags & kEmitKeys))
                     ? __ldg(&c.pos[row_of(c, ch.l, ch.s, ch.h, j)]) : 0;
     }
-    if (threadIdx.x == 0 && !ctl[1])
-      if (!wait_at_least(&A.ready[ch.slice], 1, A.dev_status)) ctl[1] = 1;
+    // thread 0 decides (the abort flag may be set by other warps at any time); everyone
+    // acts on its snapshot after the barrier
+    if (threadIdx.x == 0) {
+      if (!ctl[1] && !wait_at_least(&A.arrive[ch.slice], ch.nchunks, A.dev_status)) ctl[1] = 1;
+      __threadfence();
+      ctl[2] = ctl[1];
+    }
     epi_sync();
     if (threadIdx.x == 0) trace_ev(A, nev, 5 + 1000 * (ch.slice + 1));
-    if (ctl[1]) return false;
-    const float* fin = A.fin + (long long)ch.slice * (3 * W + kMaxWalk);
+    if (ctl[2]) return false;
+    const float* rec = merge_slice(ch);
     const float* m = mc(ch.b);
+    if (threadIdx.x == 0) {
+      // Eq. (4) in rank-1 form on <P_u, P_t> = Gram / (Z_u Z_t)
+      float gam[kMaxWalk], gsum = 0.f;
+      for (int t = 0; t < H; ++t) {
+        float g = 1.f;
+        for (int u = 0; u < t; ++u)
+          g += gam[u] * rec[2 * W + pair_index(u, t)] /
+               (rec[W + (W - H + u)] * rec[W + (W - H + t)]);
+        gam[t] = g;
+        gsum += g;
+      }
+      // ||C||_1 = sum_t gamma_t since every row P sums to one
+      for (int t = 0; t < H; ++t) cc()[t] = gam[t] / (gsum * rec[W + (W - H + t)]);
+    }
+    epi_sync();
     if (threadIdx.x < W) {
       const int w = threadIdx.x;
-      const float shift = exp2f((m[w] - __ldcg(&fin[w])) * cl2);
-      ca()[w] = __ldcg(&fin[2 * W + w]) * shift;
-      if (w >= W - H) cc()[w - (W - H)] = __ldcg(&fin[3 * W + (w - (W - H))]) * shift;
+      // fold this chunk's max shift into the final per-row weights
+      const float shift = exp2f((m[w] - rec[w]) * cl2);
+      ca()[w] = shift / ((float)W * rec[W + w]);
+      if (w >= W - H) nm()[w] = cc()[w - (W - H)] * shift;   // nm reused as scratch
     }
     if (ch.k == 0 && (A.out.flags & kEmitStats) && threadIdx.x < W) {
       const int w = threadIdx.x;
-      A.out.row_stats[((long long)ch.slice * W + w) * 2] = __ldcg(&fin[w]) * rsqrtf((float)D);
-      A.out.row_stats[((long long)ch.slice * W + w) * 2 + 1] = __ldcg(&fin[W + w]);
+      A.out.row_stats[((long long)ch.slice * W + w) * 2] = rec[w] * rsqrtf((float)D);
+      A.out.row_stats[((long long)ch.slice * W + w) * 2 + 1] = rec[W + w];
     }
     epi_sync();
+    if (threadIdx.x < W && threadIdx.x >= W - H) cc()[threadIdx.x - (W - H)] = nm()[threadIdx.x];
+    epi_sync();
     if (threadIdx.x == 0) trace_ev(A, nev, 6);
-    const uint32_t lb = lane_base(ch);
+    // partial sums over this warpgroup's columns for every tile, one barrier, then each
+    // warpgroup finalizes a quarter of the tiles
+    float sca[CW], scc[kMaxWalk];
+#pragma unroll
+    for (int i = 0; i < CW; ++i) sca[i] = ca()[col0 + i];
+#pragma unroll
+    for (int tt = 0; tt < kMaxWalk; ++tt) scc[tt] = cc()[tt];
+    const int row = lg * 32 + lane;
+    for (int t = 0; t < ch.ntiles; ++t) {
+      float v[CW];
+      tmem_ldn<CW>(taddr(ch, t), v);
+      float a4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < CW; ++i) a4[i & 3] = fmaf(v[i], sca[i], a4[i & 3]);
+      apart()[(t * 4 + wg) * kTileRows + row] = (a4[0] + a4[1]) + (a4[2] + a4[3]);
+      if (wg == 3) {
+        float ct = 0.f;
+        if (HT >= 0) {
+#pragma unroll
+          for (int tt = 0; tt < (HT > 0 ? HT : 0); ++tt) ct = fmaf(v[CW - HT + tt], scc[tt], ct);
+        } else {
+#pragma unroll
+          for (int i = 0; i < CW; ++i)
+            if (i >= CW - H) ct = fmaf(v[i], scc[(i - (CW - H)) & (kMaxWalk - 1)], ct);
+        }
+        ctp()[t * kTileRows + row] = ct;
+      }
+    }
+    epi_sync();
     const uint32_t head_id = (uint32_t)((p.layer_id_base + ch.l) * c.kv_heads + ch.h);
     const uint32_t seq_id = (uint32_t)(p.seq_id_base + ch.s);
-    const float* sca = ca();
-    const float* scc = cc();
 #pragma unroll
-    for (int r = 0; r < kMaxRows; ++r) {
-      const int t = wg + 2 * r;
+    for (int r = 0; r < 2; ++r) {
+      const int t = wg + 4 * r;
       if (t >= ch.ntiles) break;
-      const int j = ch.j0 + t * kTileRows + (warp & 3) * 32 + lane;
-      float a = 0.f, ct = 0.f;
-#pragma unroll
-      for (int cb = 0; cb < W; cb += NB) {
-        float v[NB];
-        tmem_load<NB>(lb + t * W + cb, v);
-#pragma unroll
-        for (int i = 0; i < NB; ++i) a = fmaf(v[i], sca[cb + i], a);
-        if (cb + NB == W) {
-          if (HT >= 0) {
-#pragma unroll
-            for (int tt = 0; tt < (HT > 0 ? HT : 0); ++tt) ct = fmaf(v[NB - HT + tt], scc[tt], ct);
-          } else {
-#pragma unroll
-            for (int i = NB - kMaxWalk; i < NB; ++i)
-              if (i >= NB - H) ct = fmaf(v[i], scc[i - (NB - H)], ct);
-          }
-        }
-      }
-      if (j < ch.T) {
-        const float sj = a + p.lambda * ct;
-        const float ramp = (ch.T > 1) ? (float)j / (float)(ch.T - 1) : 0.f;
-        const float wj = sj + p.eps_tie * ramp;
-        const long long o = (long long)ch.slice * c.capacity + j;
-        if (A.out.flags & kEmitA) A.out.a[o] = a;
-        if (A.out.flags & kEmitC) A.out.ctilde[o] = ct;
-        if (A.out.flags & kEmitW) A.out.w[o] = wj;
-        if (A.out.flags & kEmitKeys) {
-          uint32_t key = kForcedKey;
-          if (!(j < p.n_sink || j >= ch.T - p.n_recent))
-            key = candidate_key(wj, posv[r], p, head_id, seq_id);
-          A.out.keys[o] = key;
-        }
+      const int j = ch.j0 + t * kTileRows + row;
+      if (j >= ch.T) continue;
+      const float* ap = apart() + t * 4 * kTileRows + row;
+      const float a = (ap[0] + ap[kTileRows]) + (ap[2 * kTileRows] + ap[3 * kTileRows]);
+      const float ct = ctp()[t * kTileRows + row];
+      const float sj = a + p.lambda * ct;
+      const float ramp = (ch.T > 1) ? (float)j / (float)(ch.T - 1) : 0.f;
+      const float wj = sj + p.eps_tie * ramp;
+      const long long o = (long long)ch.slice * c.capacity + j;
+      if (A.out.flags & kEmitA) A.out.a[o] = a;
+      if (A.out.flags & kEmitC) A.out.ctilde[o] = ct;
+      if (A.out.flags & kEmitW) A.out.w[o] = wj;
+      if (A.out.flags & kEmitKeys) {
+        uint32_t key = kForcedKey;
+        if (!(j < p.n_sink || j >= ch.T - p.n_recent))
+          key = candidate_key(wj, posv[r], p, head_id, seq_id);
+        A.out.keys[o] = key;
       }
     }
     return true;
   }
 
-  // The epilogue loop. With two TMEM buffers it is software-pipelined: chunk c+1's
+  // The epilogue loop, software-pipelined when TMEM holds two or more chunks: chunk c+1's
   // statistics are computed and published before chunk c waits for its slice.
   template <int HT>
   __device__ void run(uint64_t* bar_tfull, uint64_t* bar_tempty, int chunk_rows, int nbuf) {
@@ -724,10 +766,14 @@ struct Epi {
     };
     for (long long id = next_chunk(A, blockIdx.x, chunk_rows); id >= 0;
          id = next_chunk(A, id + gridDim.x, chunk_rows), ++cnt) {
-      if (ctl[1]) break;
+      if (threadIdx.x == 0) ctl[3] = ctl[1];   // one snapshot of the abort flag for all
+      epi_sync();
+      if (ctl[3]) break;
       const Chunk ch = decode_chunk(A, id, chunk_rows, cnt, nbuf);
       if (threadIdx.x == 0) trace_ev(A, nev, 100 + ch.k);
-      const bool ok = mbar_wait(&bar_tfull[ch.b], ch.use & 1, A.dev_status);
+      if (threadIdx.x == 0) ctl[2] = mbar_wait(&bar_tfull[ch.b], ch.use & 1, A.dev_status) ? 1 : 0;
+      epi_sync();
+      const bool ok = ctl[2] != 0;
       tc_fence_after();
       if (threadIdx.x == 0) trace_ev(A, nev, 1);
       if (ok) stats<HT>(ch);
@@ -742,12 +788,14 @@ struct Epi {
         have_prev = true;
       }
     }
-    if (nbuf != 1 && have_prev && !ctl[1]) finish(prev);
+    if (threadIdx.x == 0) ctl[3] = ctl[1];
+    epi_sync();
+    if (nbuf != 1 && have_prev && !ctl[3]) finish(prev);
   }
 };
 
-// 10 warps per CTA: one SM sub-partition holds 3 of them, so the 16K-register share of a
-// sub-partition caps a thread at 168 registers.
+// 18 warps per CTA: one SM sub-partition holds 5 of them, so the 16K-register share of a
+// sub-partition caps a thread at about 100 registers.
 template <int W, int D>
 __global__ void __launch_bounds__(kThreads, 1)
 score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
@@ -755,11 +803,11 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
-  uint64_t* bar_full = reinterpret_cast<uint64_t*>(sm + S::kOffBar);   // [kStages]
-  uint64_t* bar_empty = bar_full + kStages;                           // [kStages]
-  uint64_t* bar_tfull = bar_empty + kStages;                          // [2] TMEM buffer ready
-  uint64_t* bar_tempty = bar_tfull + 2;                               // [2] TMEM buffer free
-  uint64_t* bar_qfull = bar_tempty + 2;
+  uint64_t* bar_full = reinterpret_cast<uint64_t*>(sm + S::kOffBar);   // [S::kStages]
+  uint64_t* bar_empty = bar_full + S::kStages;                           // [S::kStages]
+  uint64_t* bar_tfull = bar_empty + S::kStages;                          // [3] TMEM buffer ready
+  uint64_t* bar_tempty = bar_tfull + 3;                               // [3] TMEM buffer free
+  uint64_t* bar_qfull = bar_tempty + 3;
   uint64_t* bar_qempty = bar_qfull + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S::kOffMisc);
   int* ctl = reinterpret_cast<int*>(sm + S::kOffMisc + 16);   // [0] merge role, [1] abort
@@ -770,14 +818,14 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
   constexpr uint32_t kIdesc = idesc_bf16<W>();
   const int chunk_rows = A.tiles_per_chunk * kTileRows;
   const int nbuf = A.nbuf;
-  const uint32_t buf_cols = A.tmem_cols / (uint32_t)nbuf;
+  const uint32_t buf_cols = (A.tmem_cols / (uint32_t)nbuf / W) * W;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < S::kStages; ++i) {
       mbar_init(&bar_full[i], 1);
       mbar_init(&bar_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 3; ++i) {
       mbar_init(&bar_tfull[i], 1);
       mbar_init(&bar_tempty[i], 1);
     }
@@ -785,6 +833,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
     mbar_init(bar_qempty, 1);
     ctl[0] = 0;
     ctl[1] = 0;
+    ctl[2] = 0;
+    ctl[3] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
   }
@@ -822,7 +872,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
           prev_slice = slice;
         }
         for (int t = 0; t < ntiles; ++t, ++u) {
-          const uint32_t st = u % kStages, ph = (u / kStages) & 1;
+          const uint32_t st = u % S::kStages, ph = (u / S::kStages) & 1;
           if (!mbar_wait(&bar_empty[st], ph ^ 1, A.dev_status)) { *abort_flag = 1; break; }
           const uint32_t dst = smem_u32(sm + S::kOffK + st * S::kTileBytes);
           const int r0 = j0 + t * kTileRows;
@@ -869,7 +919,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
         }
         bool fail = false;
         for (int t = 0; t < ntiles; ++t, ++u) {
-          const uint32_t st = u % kStages, ph = (u / kStages) & 1;
+          const uint32_t st = u % S::kStages, ph = (u / S::kStages) & 1;
           if (!mbar_wait(&bar_full[st], ph, A.dev_status)) { fail = true; break; }
           tc_fence_after();
           const uint32_t ka = smem_u32(sm + S::kOffK + st * S::kTileBytes);
@@ -992,15 +1042,16 @@ cudaError_t launch_t(const nx_cache& c, const nx_params& p, const void* q, const
     // buffers (the next chunk's MMAs overlap this chunk's epilogue).
     int nbuf = 0, tpc = 0, maxc = 0;
     long long grid_sel = 0, best = -1;
-    for (int nb = 2; nb >= 1; --nb) {
-      const int max_tiles = min(16, (int)(tmem_cols / nb / W));
+    for (int nb = 3; nb >= 1; --nb) {
+      const int max_tiles = min(kMaxChunkTiles, (int)(tmem_cols / nb / W));
       for (int t = 1; t <= max_tiles; ++t) {
         const int mc = (int)((cap_tiles + t - 1) / t);
-        if (mc > grid_max || mc > kGroup * kGroup) continue;
+        if (mc > grid_max || mc > kGroup * kMaxBatches) continue;
         const long long per = grid_max / mc;                 // whole slices per round
         const long long rounds = (slices + per - 1) / per;
-        // a single buffer overlaps less; ties go to fewer rounds (fewer barrier waits)
-        long long cost = (rounds * t * (nb == 2 ? 2 : 3)) * 4096 + rounds;
+        // deeper TMEM buffering overlaps more; ties go to fewer rounds
+        const int depth_cost = nb == 3 ? 20 : (nb == 2 ? 22 : 30);
+        long long cost = (rounds * t * depth_cost) * 4096 + rounds;
         if (best < 0 || cost < best) {
           best = cost;
           nbuf = nb;
@@ -1018,12 +1069,7 @@ cudaError_t launch_t(const nx_cache& c, const nx_params& p, const void* q, const
     a.qimg = reinterpret_cast<const unsigned char*>(ws + L.qbar);
     a.tmem_cols = tmem_cols;
     a.partial = reinterpret_cast<float*>(ws + L.stats);
-    a.fin = reinterpret_cast<float*>(ws + L.fin);
     a.arrive = reinterpret_cast<int*>(ws + L.barriers);
-    a.ready = a.arrive + slices;
-    a.garrive = reinterpret_cast<int*>(ws + L.group_arrive);
-    a.grec = reinterpret_cast<float*>(ws + L.group_rec);
-    a.ngroups = L.groups_per_slice;
     a.newlen = reinterpret_cast<const int32_t*>(ws + L.newlen);
     a.out = out;
     a.dev_status = dev_status;
@@ -1079,6 +1125,7 @@ bool tc_supported(const nx_cache& c, const nx_params& p) {
   if (c.dtype != NX_DTYPE_BF16) return false;
   if (c.head_dim != 64 && c.head_dim != 128) return false;
   if (p.window != 16 && p.window != 32 && p.window != 64) return false;
+  if (p.walk_len > p.window / 4) return false;       // walk rows within one warpgroup
   if (c.page_size != 0 && c.page_size < 8) return false;
   return true;
 }
