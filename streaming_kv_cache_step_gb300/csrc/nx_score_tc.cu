@@ -32,7 +32,8 @@ constexpr int kEpiWarps = 16;          // warps 0-15: epilogue (four warpgroups)
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kProducerWarp = kEpiWarps;       // TMA producer
 constexpr int kMmaWarp = kEpiWarps + 1;        // MMA issuer, TMEM owner
-constexpr int kThreads = kEpiThreads + 64;
+constexpr int kMergeWarp = kEpiWarps + 2;      // merges each slice's chunk records
+constexpr int kThreads = kEpiThreads + 96;
 constexpr int kTileRows = 128;
 constexpr int kMaxChunkTiles = 8;      // tiles per chunk (the pass-2 partials are sized for it)
 constexpr long long kWaitLimit = 1LL << 22;   // mbarrier polls before giving up
@@ -279,72 +280,14 @@ __device__ __forceinline__ float warp_sum(float x) {
 // ---------------------------------------------------------------------------
 // Merging chunk statistics
 // ---------------------------------------------------------------------------
-constexpr int kGroup = 64;        // records merged at a time
-constexpr int kMaxBatches = 4;    // chunks per slice <= kGroup * kMaxBatches
+constexpr int kGroup = 64;        // records the merge warp copies in at a time
+constexpr int kMaxBatches = 4;    // chunks per slice <= kGroup * kMaxBatches (grid choice)
 
 // A record holds, for the rows it covers: per window row w the maximum raw logit m_w and
 // sum_j exp((l_wj - m_w)/sqrt(d)) (natural-log units), and per walk-row pair (p, q) the
-// Gram sum_j exp((l_pj - m_p)/sqrt(d)) exp((l_qj - m_q)/sqrt(d)). merge_records combines
-// n <= kGroup records (global memory, `stride` floats apart) into one record `dst` of the same
-// form, with the epilogue threads: every value is loaded into shared memory at once
-// (independent loads, one round trip), then combined in a fixed order.
-template <int W, bool GSRC>
-__device__ __forceinline__ void merge_records(const float* src, int n, int stride, float* dst,
-                                              float* stage, int H, float cl2) {
-  constexpr int R = 2 * W + kMaxPairs;
-  constexpr int PARTS = kEpiThreads / W;       // threads per window row
-  const int tid = threadIdx.x;
-  for (int idx = tid; idx < n * R; idx += kEpiThreads) {
-    const int i = idx / R, f = idx - i * R;
-    stage[idx] = GSRC ? __ldcg(&src[(long long)i * stride + f]) : src[i * stride + f];
-  }
-  float* sM = stage + kGroup * R;      // merged maxima (W <= 64 floats)
-  float* part = sM + 64;               // [PARTS][W] then [GP][kMaxPairs] partial results
-  epi_sync();
-  const int w = tid % W, pt = tid / W;
-  float m = -INFINITY;
-  for (int i = pt; i < n; i += PARTS) m = fmaxf(m, stage[i * R + w]);
-  part[pt * W + w] = m;
-  epi_sync();
-  if (tid < W) {
-    float M = part[tid];
-    for (int q = 1; q < PARTS; ++q) M = fmaxf(M, part[q * W + tid]);
-    sM[tid] = M;
-  }
-  epi_sync();
-  const float Mw = sM[w];
-  float z = 0.f;
-  for (int i = pt; i < n; i += PARTS) z += stage[i * R + W + w] * exp2f((stage[i * R + w] - Mw) * cl2);
-  part[pt * W + w] = z;
-  constexpr int GP = kEpiThreads / kMaxPairs;  // 9 parts for 28 pairs
-  float g = 0.f;
-  int pu = 0, pt2 = 0;
-  const int gi = tid % kMaxPairs, gpart = tid / kMaxPairs;
-  pair_of(gi, pu, pt2);
-  if (gpart < GP && pt2 < H) {
-    const int wp = W - H + pu, wq = W - H + pt2;
-    const float mp = sM[wp], mq = sM[wq];
-    for (int i = gpart; i < n; i += GP) {
-      const float* r = stage + i * R;
-      g += r[2 * W + gi] * exp2f(((r[wp] - mp) + (r[wq] - mq)) * cl2);
-    }
-  }
-  float* gpartial = part + PARTS * W;
-  if (gpart < GP) gpartial[gpart * kMaxPairs + gi] = g;
-  epi_sync();
-  if (tid < W) {
-    float Z = 0.f;
-    for (int q = 0; q < PARTS; ++q) Z += part[q * W + tid];
-    dst[tid] = sM[tid];
-    dst[W + tid] = Z;
-  } else if (tid >= 64 && tid < 64 + kMaxPairs) {
-    const int k = tid - 64;
-    float G = 0.f;
-    for (int q = 0; q < GP; ++q) G += gpartial[q * kMaxPairs + k];
-    dst[2 * W + k] = G;
-  }
-  epi_sync();
-}
+// Gram sum_j exp((l_pj - m_p)/sqrt(d)) exp((l_qj - m_q)/sqrt(d)). Records of one slice sit
+// contiguously in global memory, `stride` floats apart, in chunk order; the merge warp
+// below combines them in that fixed order.
 
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
@@ -367,20 +310,23 @@ struct Smem {
   static constexpr int kRedStride = W + kMaxPairs;        // one warp's partial reductions
   static constexpr int kOffK = 0;
   static constexpr int kOffQ = kStages * kTileBytes;
-  static constexpr int kOffBar = kOffQ + kQBytes;         // 16 mbarriers
-  static constexpr int kOffMisc = kOffBar + 128;          // tmem slot + control words
+  static constexpr int kOffBar = kOffQ + kQBytes;         // up to 32 mbarriers
+  static constexpr int kOffMisc = kOffBar + 256;          // tmem slot + control words
   static constexpr int kOffRed = kOffMisc + 64;           // [kEpiWarps][kRedStride]
   static constexpr int kOffMc = kOffRed + kEpiWarps * kRedStride * 4;   // [3][W] chunk maxima
   static constexpr int kOffCa = kOffMc + 3 * W * 4;       // [W] a coefficients
   static constexpr int kOffCc = kOffCa + W * 4;           // [kMaxWalk] walk coefficients
   static constexpr int kOffNm = kOffCc + kMaxWalk * 4;    // [W] -max * cl2 of the chunk
-  static constexpr int kOffRec = kOffNm + W * 4;          // [kMaxBatches + 1][kRec] merged
-  static constexpr int kOffPart = kOffRec + (kMaxBatches + 1) * kRec * 4;
+  static constexpr int kMrec = 2 * W + kMaxWalk;          // merged: max, normaliser, walk
+  static constexpr int kOffMrec = kOffNm + W * 4;         // [3][kMrec] one per TMEM buffer
+  static constexpr int kOffMs = kOffMrec + 3 * kMrec * 4; // merge warp scratch [2][W]
+  static constexpr int kOffPart = kOffMs + 2 * W * 4;
   // pass-2 partial a per tile, warpgroup and row; the walk term per tile and row
   static constexpr int kOffCt = kOffPart + kMaxChunkTiles * 4 * kTileRows * 4;
-  // merge staging: [kGroup][kRec] records, 64 maxima, partial sums
+  // merge staging: kGroup chunk records as laid out in global memory
+  static constexpr int kRecStride = (kRec + 3) / 4 * 4;
   static constexpr int kOffStage = kOffCt + kMaxChunkTiles * kTileRows * 4;
-  static constexpr int kBytes = kOffStage + (kGroup * kRec + 64 + kEpiThreads + kEpiThreads) * 4;
+  static constexpr int kBytes = kOffStage + kGroup * kRecStride * 4;
   static constexpr int kAlloc = kBytes + 1024;            // slack for 1024-byte alignment
 };
 
@@ -607,26 +553,6 @@ struct Epi {
     }
   }
 
-  // Once every chunk of the slice is counted in, merge all their records here (in batches
-  // of kGroup) into one: per window row the global maximum and normaliser, and the Gram.
-  __device__ float* merge_slice(const Chunk& ch) {
-    using S = Smem<W, D>;
-    float* stage = reinterpret_cast<float*>(sm + S::kOffStage);
-    float* out = recs() + kMaxBatches * S::kRec;
-    const float* base = A.partial + (long long)ch.slice * A.maxc * A.stride;
-    const int nb = (ch.nchunks + kGroup - 1) / kGroup;
-    if (nb == 1) {
-      merge_records<W, true>(base, ch.nchunks, A.stride, out, stage, H, cl2);
-    } else {
-      for (int b = 0; b < nb; ++b)
-        merge_records<W, true>(base + (long long)b * kGroup * A.stride,
-                               min(kGroup, ch.nchunks - b * kGroup), A.stride,
-                               recs() + b * S::kRec, stage, H, cl2);
-      merge_records<W, false>(recs(), nb, S::kRec, out, stage, H, cl2);
-    }
-    return out;
-  }
-
   // Wait for the slice, merge, then a, c~, w and the order key of every row.
   template <int HT>
   __device__ bool emit(const Chunk& ch) {
@@ -643,47 +569,31 @@ struct Epi {
       posv[r] = (t < ch.ntiles && j < ch.T && (A.out.flags & kEmitKeys))
                     ? __ldg(&c.pos[row_of(c, ch.l, ch.s, ch.h, j)]) : 0;
     }
-    // thread 0 decides (the abort flag may be set by other warps at any time); everyone
-    // acts on its snapshot after the barrier
+    // the merge warp publishes the slice's merged statistics for this TMEM buffer; thread 0
+    // waits (the abort flag may be set by other warps at any time) and everyone acts on
+    // its snapshot after the barrier
+    uint64_t* bar_mfull = reinterpret_cast<uint64_t*>(sm + S::kOffBar) + 2 * S::kStages + 8;
     if (threadIdx.x == 0) {
-      if (!ctl[1] && !wait_at_least(&A.arrive[ch.slice], ch.nchunks, A.dev_status)) ctl[1] = 1;
-      __threadfence();
+      if (!ctl[1] && !mbar_wait(&bar_mfull[ch.b], ch.use & 1, A.dev_status)) ctl[1] = 1;
       ctl[2] = ctl[1];
     }
     epi_sync();
     if (threadIdx.x == 0) trace_ev(A, nev, 5 + 1000 * (ch.slice + 1));
     if (ctl[2]) return false;
-    const float* rec = merge_slice(ch);
+    const float* mr = reinterpret_cast<const float*>(sm + S::kOffMrec) + ch.b * S::kMrec;
     const float* m = mc(ch.b);
-    if (threadIdx.x == 0) {
-      // Eq. (4) in rank-1 form on <P_u, P_t> = Gram / (Z_u Z_t)
-      float gam[kMaxWalk], gsum = 0.f;
-      for (int t = 0; t < H; ++t) {
-        float g = 1.f;
-        for (int u = 0; u < t; ++u)
-          g += gam[u] * rec[2 * W + pair_index(u, t)] /
-               (rec[W + (W - H + u)] * rec[W + (W - H + t)]);
-        gam[t] = g;
-        gsum += g;
-      }
-      // ||C||_1 = sum_t gamma_t since every row P sums to one
-      for (int t = 0; t < H; ++t) cc()[t] = gam[t] / (gsum * rec[W + (W - H + t)]);
-    }
-    epi_sync();
     if (threadIdx.x < W) {
       const int w = threadIdx.x;
-      // fold this chunk's max shift into the final per-row weights
-      const float shift = exp2f((m[w] - rec[w]) * cl2);
-      ca()[w] = shift / ((float)W * rec[W + w]);
-      if (w >= W - H) nm()[w] = cc()[w - (W - H)] * shift;   // nm reused as scratch
+      // fold this chunk's max shift into the slice's per-row weights
+      const float shift = exp2f((m[w] - mr[w]) * cl2);
+      ca()[w] = shift / ((float)W * mr[W + w]);
+      if (w >= W - H) cc()[w - (W - H)] = mr[2 * W + (w - (W - H))] * shift;
     }
     if (ch.k == 0 && (A.out.flags & kEmitStats) && threadIdx.x < W) {
       const int w = threadIdx.x;
-      A.out.row_stats[((long long)ch.slice * W + w) * 2] = rec[w] * rsqrtf((float)D);
-      A.out.row_stats[((long long)ch.slice * W + w) * 2 + 1] = rec[W + w];
+      A.out.row_stats[((long long)ch.slice * W + w) * 2] = mr[w] * rsqrtf((float)D);
+      A.out.row_stats[((long long)ch.slice * W + w) * 2 + 1] = mr[W + w];
     }
-    epi_sync();
-    if (threadIdx.x < W && threadIdx.x >= W - H) cc()[threadIdx.x - (W - H)] = nm()[threadIdx.x];
     epi_sync();
     if (threadIdx.x == 0) trace_ev(A, nev, 6);
     // partial sums over this warpgroup's columns for every tile, one barrier, then each
@@ -794,7 +704,123 @@ struct Epi {
   }
 };
 
-// 18 warps per CTA: one SM sub-partition holds 5 of them, so the 16K-register share of a
+// The merge warp: for every chunk of this CTA (in the epilogue's order), once its TMEM
+// buffer's previous user is finished and every chunk of its slice has published, pull
+// the slice's chunk records into shared memory (one bulk copy per kGroup records) and
+// merge them with an online rescale across batches: per window row the maximum and the
+// normaliser, and the walk coefficients gamma_t / (sum gamma * Z_t) of Eq. (4).
+template <int W, int D>
+__device__ void merge_warp(const Args& A, uint8_t* sm, int chunk_rows, int nbuf, float cl2,
+                           uint64_t* bar_tempty, uint64_t* bar_mfull, uint64_t* bar_htx,
+                           volatile int* abort_flag) {
+  using S = Smem<W, D>;
+  constexpr int QW = (W + 31) / 32;       // columns per lane
+  const int lane = threadIdx.x & 31;
+  const int H = A.p.walk_len;
+  float* stage = reinterpret_cast<float*>(sm + S::kOffStage);
+  float* ms = reinterpret_cast<float*>(sm + S::kOffMs);     // [0]: maxima, [1]: normalisers
+  uint32_t cnt = 0, htx = 0;
+  for (long long id = next_chunk(A, blockIdx.x, chunk_rows); id >= 0 && !*abort_flag;
+       id = next_chunk(A, id + gridDim.x, chunk_rows), ++cnt) {
+    const Chunk ch = decode_chunk(A, id, chunk_rows, cnt, nbuf);
+    int ok = 1;
+    if (lane == 0) {
+      ok = mbar_wait(&bar_tempty[ch.b], (ch.use & 1) ^ 1, A.dev_status) &&
+           wait_at_least(&A.arrive[ch.slice], ch.nchunks, A.dev_status);
+      __threadfence();
+      // the records were written through the generic proxy; the bulk copies read them
+      // through the async proxy
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) { *abort_flag = 1; break; }
+    float M[QW], Z[QW];
+#pragma unroll
+    for (int q = 0; q < QW; ++q) {
+      M[q] = -INFINITY;
+      Z[q] = 0.f;
+    }
+    float G = 0.f;                          // lane k < kMaxPairs: Gram entry k
+    int gu = 0, gt = 0;
+    pair_of(lane < kMaxPairs ? lane : 0, gu, gt);
+    const bool gact = lane < kMaxPairs && gt < H;
+    const int wp = W - H + gu, wq = W - H + gt;
+    const float* src = A.partial + (long long)ch.slice * A.maxc * A.stride;
+    for (int b0 = 0; b0 < ch.nchunks && ok; b0 += kGroup) {
+      const int n = min(kGroup, ch.nchunks - b0);
+      if (lane == 0) {
+        const uint32_t bytes = (uint32_t)(n * A.stride * 4);
+        mbar_expect_tx(bar_htx, bytes);
+        bulk_load(smem_u32(stage), src + (long long)b0 * A.stride, bytes, bar_htx);
+        ok = mbar_wait(bar_htx, htx & 1, A.dev_status);
+      }
+      ++htx;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      // new maxima, rescaled normalisers
+      float Mn[QW];
+#pragma unroll
+      for (int q = 0; q < QW; ++q) {
+        const int c = lane + 32 * q;
+        float mb = M[q];
+        if (c < W)
+          for (int i = 0; i < n; ++i) mb = fmaxf(mb, stage[i * A.stride + c]);
+        Mn[q] = mb;
+        if (c < W) {
+          float z = (M[q] == -INFINITY) ? 0.f : Z[q] * exp2f((M[q] - mb) * cl2);
+          for (int i = 0; i < n; ++i)
+            z += stage[i * A.stride + W + c] * exp2f((stage[i * A.stride + c] - mb) * cl2);
+          Z[q] = z;
+          ms[c] = mb;              // the Gram step needs every column's new maximum
+          ms[W + c] = M[q];        // and its previous one
+        }
+      }
+      __syncwarp();
+      if (gact) {
+        const float np = ms[wp], nq = ms[wq], op = ms[W + wp], oq = ms[W + wq];
+        float g = (op == -INFINITY) ? 0.f : G * exp2f(((op - np) + (oq - nq)) * cl2);
+        for (int i = 0; i < n; ++i) {
+          const float* r = stage + i * A.stride;
+          g += r[2 * W + lane] * exp2f(((r[wp] - np) + (r[wq] - nq)) * cl2);
+        }
+        G = g;
+      }
+#pragma unroll
+      for (int q = 0; q < QW; ++q) M[q] = Mn[q];
+      __syncwarp();
+    }
+    if (!ok) { *abort_flag = 1; break; }
+    float* out = reinterpret_cast<float*>(sm + S::kOffMrec) + ch.b * S::kMrec;
+#pragma unroll
+    for (int q = 0; q < QW; ++q) {
+      const int c = lane + 32 * q;
+      if (c < W) {
+        out[c] = M[q];
+        out[W + c] = Z[q];
+        ms[W + c] = Z[q];
+      }
+    }
+    __syncwarp();
+    // Eq. (4) in rank-1 form: gamma_t = 1 + sum_{u<t} gamma_u <P_t, P_u>, with
+    // <P_u, P_t> = Gram / (Z_u Z_t); ||C||_1 = sum_t gamma_t (every row sums to one)
+    const float gnorm = gact ? G / (ms[W + wp] * ms[W + wq]) : 0.f;
+    float gam = 0.f, gsum = 0.f;               // lane t < H holds gamma_t
+    for (int t = 0; t < H; ++t) {
+      const float nt = __shfl_sync(0xffffffffu, gnorm, pair_index(lane < t ? lane : 0, t > 0 ? t : 1));
+      float v = (lane < t) ? gam * nt : 0.f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      const float g = 1.f + v;
+      if (lane == t) gam = g;
+      gsum += g;
+    }
+    if (lane < H) out[2 * W + lane] = gam / (gsum * ms[W + (W - H + lane)]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar_mfull[ch.b]);
+  }
+}
+
+// 19 warps per CTA: one SM sub-partition holds 5 of them, so the 16K-register share of a
 // sub-partition caps a thread at about 100 registers.
 template <int W, int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -809,6 +835,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
   uint64_t* bar_tempty = bar_tfull + 3;                               // [3] TMEM buffer free
   uint64_t* bar_qfull = bar_tempty + 3;
   uint64_t* bar_qempty = bar_qfull + 1;
+  uint64_t* bar_mfull = bar_full + 2 * S::kStages + 8;                 // [3] merged stats ready
+  uint64_t* bar_htx = bar_mfull + 3;                                  // merge warp's copies
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S::kOffMisc);
   int* ctl = reinterpret_cast<int*>(sm + S::kOffMisc + 16);   // [0] merge role, [1] abort
 
@@ -831,6 +859,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
     }
     mbar_init(bar_qfull, 1);
     mbar_init(bar_qempty, 1);
+    for (int i = 0; i < 3; ++i) mbar_init(&bar_mfull[i], 1);
+    mbar_init(bar_htx, 1);
     ctl[0] = 0;
     ctl[1] = 0;
     ctl[2] = 0;
@@ -945,8 +975,11 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
           mma_commit(bar_qempty);          // the query image may be replaced after these
       }
     }
+  } else if (warp == kMergeWarp) {
+    // =================== slice merge ===================
+    merge_warp<W, D>(A, sm, chunk_rows, nbuf, cl2, bar_tempty, bar_mfull, bar_htx, abort_flag);
   } else {
-    // =================== epilogue: warps 0-7 ===================
+    // =================== epilogue: warps 0-15 ===================
     Epi<W, D> epi(A, sm, tmem, buf_cols, cl2, A.p.walk_len);
     switch (A.p.walk_len) {
       case 3: epi.template run<3>(bar_tfull, bar_tempty, chunk_rows, nbuf); break;
