@@ -53,6 +53,9 @@ def parse_args():
     ap.add_argument("--workload", default="llama3_8b_layer")
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--launch", choices=("graph", "eager"), default="graph",
+                    help="device-timed loop: replay one CUDA-graph capture of the "
+                         "nexus_evict_step call, or call it eagerly every step")
     return ap.parse_args()
 
 
@@ -201,13 +204,18 @@ def run_native(args, rank, world, local):
     keep = torch.full((cache.n_slices, wl.capacity), -1, dtype=torch.int32, device=dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    clean = torch.ones(2 * l2 // 4, dtype=torch.float32, device=dev)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     names = ("k", "v", "pos", "lens")
 
     def restore():
         for n in names:
             work[n].copy_(pristine[n], non_blocking=True)
+        # evict L2: write a buffer twice its size, then read another one as large, so the
+        # step starts with a cold L2 that holds no dirty lines to write back
         flush.zero_()
+        torch.sum(clean, 0, out=sink)
 
     def step(events=None):
         arr = nexus.profile_next_call(events) if events else None
@@ -224,40 +232,79 @@ def run_native(args, rank, world, local):
     scorer_cfg = nexus.scorer_config() if "score_tc" in launch_names else None
 
     # ---- timed region ----
+    # Each timed step: restore the pristine cache, flush L2, then keep the device busy
+    # while the host issues the step, so that the events time the device work.
+    def timed(K, graph):
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        per = [[] for _ in range(nl)]
+        count = 0
+        if graph is not None:
+            g, kev_g = graph
+        for i in range(K):
+            restore()
+            torch.cuda._sleep(200_000)
+            starts[i].record(stream)
+            if graph is not None:
+                g.replay()
+            else:
+                kev_g = [torch.cuda.Event(enable_timing=True) for _ in range(nl)]
+                step(kev_g)
+            ends[i].record(stream)
+            count += nl if graph is not None else nexus.last_launch_count()
+            ends[i].synchronize()          # the graph's events are re-recorded next step
+            for j in range(nl):
+                prev = starts[i] if j == 0 else kev_g[j - 1]
+                per[j].append(prev.elapsed_time(kev_g[j]))
+        torch.cuda.synchronize()
+        step_ms = [starts[i].elapsed_time(ends[i]) for i in range(K)]
+        per_kernel = {f"{j}:{name}": statistics.mean(per[j]) * 1e3
+                      for j, name in enumerate(launch_names)}       # microseconds
+        return step_ms, per_kernel, count
+
+    graph = None
+    if args.launch == "graph":
+        # one capture of the C-ABI call, its per-launch events included; every replay
+        # runs the same kernels on the restored inputs
+        kev_g = [torch.cuda.Event(enable_timing=True) for _ in range(nl)]
+        for e in kev_g:
+            e.record(stream)
+        restore()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            arr = nexus.profile_next_call(kev_g)
+            nexus.evict_step(cache, q, params, keep, ws, status)
+            del arr
+        torch.cuda.synchronize()
+        graph = (g, kev_g)
+        for _ in range(2):
+            restore()
+            g.replay()
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0, f"device status {int(status.item())}"
+
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
     K = args.steps
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(nl)] for _ in range(K)]
-    launches = 0
     barrier(world)
     torch.cuda.synchronize()
-    for i in range(K):
-        restore()
-        # keep the device busy while the host issues the step, so the events time the
-        # kernels and not the host's launch latency
-        torch.cuda._sleep(200_000)
-        starts[i].record(stream)
-        step(kev[i])
-        ends[i].record(stream)
-        launches += nexus.last_launch_count()
+    step_ms, per_kernel, launches = timed(K, graph)
     torch.cuda.synchronize()
     barrier(world)
     time.sleep(0.2)
     clocks = sampler.stop()
     assert int(status.item()) == 0, f"device status {int(status.item())}"
-
-    step_ms = [starts[i].elapsed_time(ends[i]) for i in range(K)]
     total_ms = allmax(sum(step_ms), world)
-    per_kernel = {}
-    for j, name in enumerate(launch_names):
-        t = []
-        for i in range(K):
-            prev = starts[i] if j == 0 else kev[i][j - 1]
-            t.append(prev.elapsed_time(kev[i][j]))
-        per_kernel[f"{j}:{name}"] = statistics.mean(t) * 1e3   # microseconds
+    eager = None
+    if graph is not None:
+        # the same step called eagerly through the C ABI (host launch latency included
+        # wherever the device outruns the host)
+        ke = min(K, 30)
+        e_ms, e_kern, _ = timed(ke, None)
+        eager = dict(ms_per_step=round(allmax(sum(e_ms), world) / ke, 5), steps=ke,
+                     kernels_us={k: round(v, 3) for k, v in e_kern.items()})
 
     # algorithmic bytes of this step (from the kept-slot lists of the last step)
     lens0 = pristine["lens"].reshape(-1).cpu().numpy()
@@ -304,6 +351,7 @@ def run_native(args, rank, world, local):
     torch.cuda.synchronize()
     for i in range(e2e_steps):
         flush.zero_()
+        torch.sum(clean, 0, out=sink)
         e_s[i].record(stream)
         for n in names:
             work[n].copy_(host[n], non_blocking=True)
@@ -326,13 +374,16 @@ def run_native(args, rank, world, local):
                            window=wl.window, walk=wl.walk_len, n_sink=wl.n_sink,
                            n_recent=wl.n_recent, rows_per_step=rows_per_step,
                            moved_rows=ab["moved"], alg_bytes_per_step=ab["total"],
-                           l2="flushed between timed steps (2x L2 written)",
+                           l2="flushed between timed steps (2x L2 written, then 2x L2 read)",
+                           launch=("one CUDA-graph capture of the nexus_evict_step call, "
+                                   "replayed every step" if graph is not None
+                                   else "nexus_evict_step called every step"),
                            parallelism=f"dp{world} (independent sequences per rank)"),
                roofline=roofline,
                e2e=dict(value=round(e2e_value, 1), unit=UNIT, h2d_bytes_per_step=h2d,
                         d2h_bytes_per_step=d2h, steps=e2e_steps),
                gpu_launches=launches, kernels_us={k: round(v, 3) for k, v in per_kernel.items()},
-               scorer=scorer_cfg,
+               scorer=scorer_cfg, eager=eager,
                clocks=clocks)
     return out, wl
 

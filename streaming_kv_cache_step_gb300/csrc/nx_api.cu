@@ -151,8 +151,17 @@ void begin_call() {
 
 void note_launch(cudaStream_t st, int* launches, const char* name) {
   if (*launches < kMaxLaunchNames) g_launch_names[*launches] = name;
-  if (g_prof_active && *launches < g_prof_n && g_prof_events[*launches])
-    cudaEventRecord(reinterpret_cast<cudaEvent_t>(g_prof_events[*launches]), st);
+  // Inside a stream capture the records must be external to become event-record nodes
+  // of the graph (so that replays time the launches too).
+  if (g_prof_active && *launches < g_prof_n && g_prof_events[*launches]) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaStreamIsCapturing(st, &cs);
+    cudaEvent_t ev = reinterpret_cast<cudaEvent_t>(g_prof_events[*launches]);
+    if (cs == cudaStreamCaptureStatusActive)
+      cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal);
+    else
+      cudaEventRecord(ev, st);
+  }
   *launches += 1;
 }
 

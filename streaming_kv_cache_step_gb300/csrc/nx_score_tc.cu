@@ -55,6 +55,7 @@ struct Args {
   int maxc;                // chunk ids per slice
   int stride;              // floats per partial record
   long long total_ids;     // slices * maxc
+  int slices;
 };
 
 // ---------------------------------------------------------------------------
@@ -330,18 +331,69 @@ struct Smem {
   static constexpr int kAlloc = kBytes + 1024;            // slack for 1024-byte alignment
 };
 
-// Next chunk id >= id (stepping by the grid) that has work, or -1. Every role of a CTA
-// walks the same sequence.
-__device__ __forceinline__ long long next_chunk(const Args& A, long long id, int chunk_rows) {
-  for (; id < A.total_ids; id += gridDim.x) {
-    const int slice = (int)(id / A.maxc);
-    const int k = (int)(id % A.maxc);
-    if (A.newlen[slice] < 0) continue;
-    const int T = A.c.lens[slice];
-    if (k * chunk_rows >= T) continue;
-    return id;
+// The chunk schedule. The chunks of all slices are numbered in slice order (a slice that
+// is empty or was rejected has none), and chunk number x goes to CTA x mod grid. As a
+// slice has at most grid chunks, a CTA holds at most one chunk of any slice, and it takes
+// its chunks in increasing slice order: that keeps the slice barrier deadlock-free (the
+// earliest unfinished slice never waits on a later one), and however ragged the lengths,
+// the CTAs' chunk counts differ by at most one. Every warp of every role walks the same
+// sequence itself, warp-collectively: 32 slices at a time, one per lane, with a warp
+// scan of their chunk counts.
+struct Sched {
+  long long first;   // chunk number of the first chunk of slice `base`
+  int base;          // first slice of the current batch
+  uint32_t mask;     // lanes whose slice has a chunk for this CTA
+  int k, T;          // this lane's slice: the chunk index for this CTA, its length
+};
+
+__device__ __forceinline__ void sched_init(Sched& S) {
+  S.first = 0;
+  S.base = -32;
+  S.mask = 0;
+  S.k = 0;
+  S.T = 0;
+}
+
+// Warp-collective: the next chunk of this CTA; false once there is none.
+__device__ __forceinline__ bool sched_next(const Args& A, Sched& S, int chunk_rows,
+                                           int& slice, int& k, int& T) {
+  const int lane = threadIdx.x & 31;
+  while (S.mask == 0) {
+    S.base += 32;
+    if (S.base >= A.slices) return false;
+    const int sl = S.base + lane;
+    int t = 0, n = 0;
+    if (sl < A.slices && __ldg(&A.newlen[sl]) >= 0) {
+      t = __ldg(&A.c.lens[sl]);
+      n = (t + chunk_rows - 1) / chunk_rows;
+    }
+    int incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const long long f = S.first + (incl - n);
+    int kk = (int)blockIdx.x - (int)(f % gridDim.x);
+    if (kk < 0) kk += (int)gridDim.x;
+    S.k = kk;
+    S.T = t;
+    S.mask = __ballot_sync(0xffffffffu, kk < n);
+    S.first += __shfl_sync(0xffffffffu, incl, 31);
   }
-  return -1;
+  const int j = __ffs(S.mask) - 1;
+  S.mask &= S.mask - 1;
+  slice = S.base + j;
+  k = __shfl_sync(0xffffffffu, S.k, j);
+  T = __shfl_sync(0xffffffffu, S.T, j);
+  return true;
+}
+
+// A flag that any thread may set, read by lane 0 and broadcast (warp-uniform).
+__device__ __forceinline__ int warp_flag(volatile int* f) {
+  int v = 0;
+  if ((threadIdx.x & 31) == 0) v = *f;
+  return __shfl_sync(0xffffffffu, v, 0);
 }
 
 constexpr int kTraceEvents = 1024;
@@ -353,13 +405,22 @@ __device__ __forceinline__ long long global_ns() {
 }
 
 // Phase trace (diagnostics, off unless a buffer is installed): event e of this CTA gets
-// (tag, globaltimer ns).
+// (tag, globaltimer ns); the last three slots hold kernel-level marks.
 __device__ __forceinline__ void trace_ev(const Args& A, int& n, int tag) {
-  if (A.trace && n < kTraceEvents) {
+  if (A.trace && n < kTraceEvents - 3) {
     long long* t = A.trace + ((long long)blockIdx.x * kTraceEvents + n) * 2;
     t[0] = tag;
     t[1] = global_ns();
     ++n;
+  }
+}
+
+// kernel-level marks in the last three trace slots of the CTA: entry, setup done, exit
+__device__ __forceinline__ void trace_mark(const Args& A, int slot, int tag) {
+  if (A.trace) {
+    long long* t = A.trace + ((long long)blockIdx.x * kTraceEvents + kTraceEvents - 3 + slot) * 2;
+    t[0] = tag;
+    t[1] = global_ns();
   }
 }
 
@@ -374,12 +435,12 @@ struct Chunk {
   uint32_t use;        // how many times this buffer was used before
 };
 
-__device__ __forceinline__ Chunk decode_chunk(const Args& A, long long id, int chunk_rows,
-                                              uint32_t cc, int nbuf) {
+__device__ __forceinline__ Chunk make_chunk(const Args& A, int slice, int k, int T,
+                                            int chunk_rows, uint32_t cc, int nbuf) {
   Chunk ch;
-  ch.slice = (int)(id / A.maxc);
-  ch.k = (int)(id % A.maxc);
-  ch.T = A.c.lens[ch.slice];
+  ch.slice = slice;
+  ch.k = k;
+  ch.T = T;
   ch.nchunks = (ch.T + chunk_rows - 1) / chunk_rows;
   ch.j0 = ch.k * chunk_rows;
   ch.ntiles = min(A.tiles_per_chunk, (ch.T - ch.j0 + kTileRows - 1) / kTileRows);
@@ -674,12 +735,14 @@ struct Epi {
       }
       return ok;
     };
-    for (long long id = next_chunk(A, blockIdx.x, chunk_rows); id >= 0;
-         id = next_chunk(A, id + gridDim.x, chunk_rows), ++cnt) {
+    Sched sc;
+    sched_init(sc);
+    int sl, kq, Tq;
+    for (; sched_next(A, sc, chunk_rows, sl, kq, Tq); ++cnt) {
       if (threadIdx.x == 0) ctl[3] = ctl[1];   // one snapshot of the abort flag for all
       epi_sync();
       if (ctl[3]) break;
-      const Chunk ch = decode_chunk(A, id, chunk_rows, cnt, nbuf);
+      const Chunk ch = make_chunk(A, sl, kq, Tq, chunk_rows, cnt, nbuf);
       if (threadIdx.x == 0) trace_ev(A, nev, 100 + ch.k);
       if (threadIdx.x == 0) ctl[2] = mbar_wait(&bar_tfull[ch.b], ch.use & 1, A.dev_status) ? 1 : 0;
       epi_sync();
@@ -720,9 +783,11 @@ __device__ void merge_warp(const Args& A, uint8_t* sm, int chunk_rows, int nbuf,
   float* stage = reinterpret_cast<float*>(sm + S::kOffStage);
   float* ms = reinterpret_cast<float*>(sm + S::kOffMs);     // [0]: maxima, [1]: normalisers
   uint32_t cnt = 0, htx = 0;
-  for (long long id = next_chunk(A, blockIdx.x, chunk_rows); id >= 0 && !*abort_flag;
-       id = next_chunk(A, id + gridDim.x, chunk_rows), ++cnt) {
-    const Chunk ch = decode_chunk(A, id, chunk_rows, cnt, nbuf);
+  Sched sc;
+  sched_init(sc);
+  int sl, kq, Tq;
+  for (; !warp_flag(abort_flag) && sched_next(A, sc, chunk_rows, sl, kq, Tq); ++cnt) {
+    const Chunk ch = make_chunk(A, sl, kq, Tq, chunk_rows, cnt, nbuf);
     int ok = 1;
     if (lane == 0) {
       ok = mbar_wait(&bar_tempty[ch.b], (ch.use & 1) ^ 1, A.dev_status) &&
@@ -849,6 +914,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
   const uint32_t buf_cols = (A.tmem_cols / (uint32_t)nbuf / W) * W;
 
   if (threadIdx.x == 0) {
+    trace_mark(A, 0, 7);
     for (int i = 0; i < S::kStages; ++i) {
       mbar_init(&bar_full[i], 1);
       mbar_init(&bar_empty[i], 1);
@@ -879,31 +945,35 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   volatile int* abort_flag = ctl + 1;
+  if (threadIdx.x == 0) trace_mark(A, 1, 9);
 
   if (warp == kProducerWarp) {
     // =================== TMA producer: query images and K tiles ===================
-    if (lane == 0) {
-      uint32_t u = 0, qn = 0;
-      int prev_slice = -1;
-      for (long long id = next_chunk(A, blockIdx.x, chunk_rows); id >= 0 && !*abort_flag;
-           id = next_chunk(A, id + gridDim.x, chunk_rows)) {
-        const int slice = (int)(id / A.maxc), k = (int)(id % A.maxc);
-        const int T = c.lens[slice];
+    uint32_t u = 0, qn = 0;
+    int prev_slice = -1;
+    Sched sc;
+    sched_init(sc);
+    int slice, k, T;
+    while (!warp_flag(abort_flag) && sched_next(A, sc, chunk_rows, slice, k, T)) {
+      int fail = 0;
+      if (lane == 0) {
         int l, s, h;
         slice_coords(c, slice, l, s, h);
         const int j0 = k * chunk_rows;
         const int ntiles = min(A.tiles_per_chunk, (T - j0 + kTileRows - 1) / kTileRows);
         if (slice != prev_slice) {
-          if (qn > 0 && !mbar_wait(bar_qempty, (qn - 1) & 1, A.dev_status)) { *abort_flag = 1; break; }
-          mbar_expect_tx(bar_qfull, S::kQBytes);
-          bulk_load(smem_u32(sm + S::kOffQ), A.qimg + (long long)slice * S::kQBytes, S::kQBytes,
-                    bar_qfull);
-          ++qn;
-          prev_slice = slice;
+          if (qn > 0 && !mbar_wait(bar_qempty, (qn - 1) & 1, A.dev_status)) fail = 1;
+          if (!fail) {
+            mbar_expect_tx(bar_qfull, S::kQBytes);
+            bulk_load(smem_u32(sm + S::kOffQ), A.qimg + (long long)slice * S::kQBytes,
+                      S::kQBytes, bar_qfull);
+            ++qn;
+            prev_slice = slice;
+          }
         }
-        for (int t = 0; t < ntiles; ++t, ++u) {
+        for (int t = 0; t < ntiles && !fail; ++t, ++u) {
           const uint32_t st = u % S::kStages, ph = (u / S::kStages) & 1;
-          if (!mbar_wait(&bar_empty[st], ph ^ 1, A.dev_status)) { *abort_flag = 1; break; }
+          if (!mbar_wait(&bar_empty[st], ph ^ 1, A.dev_status)) { fail = 1; break; }
           const uint32_t dst = smem_u32(sm + S::kOffK + st * S::kTileBytes);
           const int r0 = j0 + t * kTileRows;
           if (c.page_size == 0) {
@@ -925,32 +995,36 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
             }
           }
         }
+        if (fail) *abort_flag = 1;
       }
+      if (__shfl_sync(0xffffffffu, fail, 0)) break;
     }
   } else if (warp == kMmaWarp) {
     // =================== MMA issuer ===================
-    if (lane == 0) {
-      uint32_t u = 0, qn = 0, cc = 0;
-      int prev_slice = -1;
-      const uint32_t qa = smem_u32(sm + S::kOffQ);
-      for (long long id = next_chunk(A, blockIdx.x, chunk_rows); id >= 0 && !*abort_flag;
-           id = next_chunk(A, id + gridDim.x, chunk_rows), ++cc) {
-        const int slice = (int)(id / A.maxc), k = (int)(id % A.maxc);
-        const int T = c.lens[slice];
+    uint32_t u = 0, qn = 0, cc = 0;
+    int prev_slice = -1;
+    const uint32_t qa = smem_u32(sm + S::kOffQ);
+    Sched sc;
+    sched_init(sc);
+    int slice, k, T;
+    for (; !warp_flag(abort_flag) && sched_next(A, sc, chunk_rows, slice, k, T); ++cc) {
+      int fail = 0;
+      if (lane == 0) {
         const int j0 = k * chunk_rows;
         const int ntiles = min(A.tiles_per_chunk, (T - j0 + kTileRows - 1) / kTileRows);
         const uint32_t b = cc % nbuf, use = cc / nbuf;
-        if (!mbar_wait(&bar_tempty[b], (use & 1) ^ 1, A.dev_status)) { *abort_flag = 1; break; }
+        // the previous slice's query image may be replaced once its MMAs are done
+        if (slice != prev_slice && prev_slice >= 0) mma_commit(bar_qempty);
+        if (!mbar_wait(&bar_tempty[b], (use & 1) ^ 1, A.dev_status)) fail = 1;
         tc_fence_after();
-        if (slice != prev_slice) {
-          if (!mbar_wait(bar_qfull, qn & 1, A.dev_status)) { *abort_flag = 1; break; }
+        if (!fail && slice != prev_slice) {
+          if (!mbar_wait(bar_qfull, qn & 1, A.dev_status)) fail = 1;
           ++qn;
           prev_slice = slice;
         }
-        bool fail = false;
-        for (int t = 0; t < ntiles; ++t, ++u) {
+        for (int t = 0; t < ntiles && !fail; ++t, ++u) {
           const uint32_t st = u % S::kStages, ph = (u / S::kStages) & 1;
-          if (!mbar_wait(&bar_full[st], ph, A.dev_status)) { fail = true; break; }
+          if (!mbar_wait(&bar_full[st], ph, A.dev_status)) { fail = 1; break; }
           tc_fence_after();
           const uint32_t ka = smem_u32(sm + S::kOffK + st * S::kTileBytes);
           const uint32_t dt = tmem + b * buf_cols + (uint32_t)(t * W);
@@ -968,12 +1042,10 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
           }
           mma_commit(&bar_empty[st]);      // the stage's smem is free once these finish
         }
-        if (fail) { *abort_flag = 1; break; }
-        mma_commit(&bar_tfull[b]);         // the chunk's logits are in TMEM buffer b
-        const long long nid = next_chunk(A, id + gridDim.x, chunk_rows);
-        if (nid >= 0 && (int)(nid / A.maxc) != slice)
-          mma_commit(bar_qempty);          // the query image may be replaced after these
+        if (!fail) mma_commit(&bar_tfull[b]);   // the chunk's logits are in TMEM buffer b
+        if (fail) *abort_flag = 1;
       }
+      if (__shfl_sync(0xffffffffu, fail, 0)) break;
     }
   } else if (warp == kMergeWarp) {
     // =================== slice merge ===================
@@ -995,6 +1067,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(A.tmem_cols));
   }
+  if (threadIdx.x == 0) trace_mark(A, 2, 8);
 }
 
 // ---------------------------------------------------------------------------
@@ -1111,6 +1184,7 @@ cudaError_t launch_t(const nx_cache& c, const nx_params& p, const void* q, const
     a.maxc = maxc;
     a.stride = L.stats_stride;
     a.total_ids = slices * maxc;
+    a.slices = (int)slices;
     a.trace = g_trace;
     const long long grid = a.total_ids < grid_sel ? a.total_ids : grid_sel;
 

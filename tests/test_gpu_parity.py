@@ -246,3 +246,36 @@ def test_tensor_core_scorer_matches_cuda_core_scorer(name):
         T = int(lens[sid])
         assert np.all(np.abs(w_tc[sid, :T] - w_si[sid, :T]) <= 2 * score_tol(w_si[sid, :T], T))
         assert np.all(np.abs(c_tc[sid, :T] - c_si[sid, :T]) <= 2 * score_tol(c_si[sid, :T], T))
+
+
+@pytest.mark.parametrize("name", ["gqa_ragged", "paged"])
+def test_evict_step_replays_from_a_cuda_graph(name):
+    """nexus_evict_step captured once in a CUDA graph and replayed on the restored cache
+    gives, every replay, exactly what the eager call gives."""
+    wl = CASES[name]
+    run = GpuRun(wl)
+    pristine = {k: run.d[k].clone() for k in ("k", "v", "pos", "lens")}
+
+    def restore():
+        for k, t in pristine.items():
+            run.d[k].copy_(t)
+
+    run.keep.fill_(-1)
+    nexus.evict_step(run.cache, run.q, run.params, run.keep, run.ws, run.status)
+    run.check_status()
+    want = {k: run.d[k].clone() for k in pristine}
+    want_keep = run.keep.clone()
+    restore()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        nexus.evict_step(run.cache, run.q, run.params, run.keep, run.ws, run.status)
+    for _ in range(3):
+        restore()
+        run.keep.fill_(-1)
+        g.replay()
+        torch.cuda.synchronize()
+        run.check_status()
+        assert torch.equal(run.keep, want_keep)
+        for k in pristine:
+            assert torch.equal(run.d[k], want[k]), k
