@@ -224,15 +224,26 @@ nx_status nexus_debug_compact(nx_cache* cache, const int32_t* keep_idx, const nx
 void nexus_debug_force_simt(int32_t on);
 
 /*
+ * Testing hook: the tensor-core scorer's layout, process-wide. teams = 2 asks for two
+ * independent pipelines per CTA (256 TMEM columns and eight epilogue warps each), 1 for
+ * one pipeline per CTA (512 columns, sixteen epilogue warps), any other value for the
+ * automatic choice (two for windows of up to 32 rows). Windows of 64 rows always take one.
+ * When the two-pipeline layout cannot run, the automatic choice falls back to one and an
+ * explicit 2 to the CUDA-core scorer.
+ */
+void nexus_debug_scorer_layout(int32_t teams);
+
+/*
  * Diagnostics of the tensor-core scorer (not part of the method):
  * nexus_debug_set_trace installs a device buffer of grid x 1024 x 2 int64 that later
- * launches fill with (phase tag, globaltimer ns) pairs per CTA; NULL turns it off.
+ * launches fill with (phase tag, globaltimer ns) pairs per pipeline; NULL turns it off.
  * nexus_debug_scorer_config writes the last launch's configuration from this host
- * thread: CTAs per SM used, per SM reported by the occupancy API, grid, tiles per chunk,
- * TMEM buffers, chunks per slice, TMEM columns, dynamic shared memory bytes. When the
- * last call could not use the tensor-core scorer, the first entry is negative: -1 no
- * tensor-map encoder, -2 too many rows for one tensor map, -3 tensor map rejected,
- * -4 a slice has more chunks than co-resident CTAs, -5 the cooperative launch did not fit.
+ * thread: pipelines per CTA, CTAs per SM reported by the occupancy API, grid (CTAs),
+ * tiles per chunk, TMEM buffers per pipeline, chunks per slice, TMEM columns per pipeline,
+ * dynamic shared memory bytes. When the last call could not use the tensor-core scorer,
+ * the first entry is negative: -1 no tensor-map encoder, -2 too many rows for one tensor
+ * map, -3 tensor map rejected, -4 a slice has more chunks than co-resident pipelines,
+ * -5 the cooperative launch did not fit, -6 no CTA fits on an SM.
  */
 void nexus_debug_set_trace(long long* device_buffer);
 void nexus_debug_scorer_config(int32_t* out8);

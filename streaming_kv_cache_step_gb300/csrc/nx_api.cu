@@ -312,6 +312,10 @@ int32_t nexus_last_launch_count(void) { return g_last_launches; }
 
 void nexus_debug_force_simt(int32_t on) { g_force_simt = on != 0; }
 
+void nexus_debug_scorer_layout(int32_t teams) {
+  nx::tc_set_layout(teams == 1 || teams == 2 ? teams : 0);
+}
+
 void nexus_debug_set_trace(long long* device_buffer) { tc_set_trace(device_buffer); }
 
 void nexus_debug_scorer_config(int32_t* out8) {

@@ -203,6 +203,7 @@ cudaError_t launch_prep(const nx_cache& c, const void* q, const nx_params& p, co
 // nx_score_tc.cu: *used is false when the shape is not covered (the caller falls back)
 bool tc_supported(const nx_cache& c, const nx_params& p);
 void tc_set_trace(long long* buf);
+void tc_set_layout(int teams);
 void tc_last_config(int32_t* out);
 cudaError_t launch_score_tc(const nx_cache& c, const nx_params& p, const void* q,
                             const WsLayout& L, char* ws, const ScoreOut& out,

@@ -28,14 +28,29 @@
 namespace nx {
 namespace tc {
 
-constexpr int kEpiWarps = 16;          // warps 0-15: epilogue (four warpgroups)
-constexpr int kEpiThreads = kEpiWarps * 32;
-constexpr int kProducerWarp = kEpiWarps;       // TMA producer
-constexpr int kMmaWarp = kEpiWarps + 1;        // MMA issuer, TMEM owner
-constexpr int kMergeWarp = kEpiWarps + 2;      // merges each slice's chunk records
-constexpr int kThreads = kEpiThreads + 96;
+// A CTA holds one or two teams; each team is a complete pipeline of its own (its own
+// chunks, shared-memory region, barriers and half of TMEM) and acts as one "virtual CTA"
+// of the chunk schedule. Warp roles of a team whose epilogue has NWG warpgroups: warps
+// [0, 4 NWG) run the epilogue, then come the TMA producer, the MMA issuer, the merge warp
+// and the publisher. NWG = 4: one team holding all 512 TMEM columns. NWG = 2: two teams of
+// 256 columns each, whose epilogues fill one another's waits (a kernel that allocates
+// TMEM runs one CTA per SM, so the overlap has to come from inside the CTA).
+template <int NWG>
+struct Roles {
+  static constexpr int kEpiWarps = 4 * NWG;
+  static constexpr int kEpiThreads = kEpiWarps * 32;
+  static constexpr int kProducerWarp = kEpiWarps;
+  static constexpr int kMmaWarp = kEpiWarps + 1;
+  static constexpr int kMergeWarp = kEpiWarps + 2;
+  static constexpr int kPublishWarp = kEpiWarps + 3;
+  static constexpr int kThreads = kEpiThreads + 128;          // one team
+  static constexpr int kTeams = NWG == 2 ? 2 : 1;
+  static constexpr int kBlockThreads = kTeams * kThreads;
+  static constexpr uint32_t kTmemCols = 512u / kTeams;      // one team's share
+  static constexpr int kMaxChunkTiles = 2 * NWG;   // the pass-2 partials are sized for it
+  static constexpr int kGroup = 32;                // records per bulk copy of the merge
+};
 constexpr int kTileRows = 128;
-constexpr int kMaxChunkTiles = 8;      // tiles per chunk (the pass-2 partials are sized for it)
 constexpr long long kWaitLimit = 1LL << 22;   // mbarrier polls before giving up
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -208,6 +223,24 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
       : "memory");
 }
 
+// N (4, 8 or 16) consecutive TMEM columns of this thread's lane, issued without a wait
+// (tmem_ld_wait() makes them usable).
+template <int N>
+__device__ __forceinline__ void tmem_ld_issue(uint32_t taddr, uint32_t* r) {
+  if constexpr (N == 4) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr));
+  } else if constexpr (N == 8) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+  } else {
+    tmem_ld16_nowait(taddr, r);
+  }
+}
+
 // N (4, 8 or 16) consecutive TMEM columns of this thread's lane, loaded and awaited.
 template <int N>
 __device__ __forceinline__ void tmem_ldn(uint32_t taddr, float* v) {
@@ -253,9 +286,10 @@ __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// Named barrier of the epilogue warps (barrier 1; __syncthreads uses barrier 0).
-__device__ __forceinline__ void epi_sync() {
-  asm volatile("bar.sync 1, %0;" ::"r"(kEpiThreads) : "memory");
+// Named barrier of a team's epilogue warps (barrier 1 + team; __syncthreads uses 0).
+template <int NWG>
+__device__ __forceinline__ void epi_sync(int bar_id) {
+  asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "n"(Roles<NWG>::kEpiThreads) : "memory");
 }
 
 __device__ __forceinline__ float warp_max(float x) {
@@ -281,8 +315,7 @@ __device__ __forceinline__ float warp_sum(float x) {
 // ---------------------------------------------------------------------------
 // Merging chunk statistics
 // ---------------------------------------------------------------------------
-constexpr int kGroup = 64;        // records the merge warp copies in at a time
-constexpr int kMaxBatches = 4;    // chunks per slice <= kGroup * kMaxBatches (grid choice)
+constexpr int kMaxChunksPerSlice = 256;   // grid choice
 
 // A record holds, for the rows it covers: per window row w the maximum raw logit m_w and
 // sum_j exp((l_wj - m_w)/sqrt(d)) (natural-log units), and per walk-row pair (p, q) the
@@ -299,9 +332,12 @@ __device__ __forceinline__ float ex2_approx(float x) {
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
-template <int W, int D>
+template <int W, int D, int NWG>
 struct Smem {
-  static constexpr int kStages = (W == 64) ? 3 : 4;       // K tiles in flight
+  using R = Roles<NWG>;
+  // K tiles in flight: 128-160 KB of them per SM
+  static constexpr int kStages =
+      NWG == 4 ? (D == 128 ? (W == 64 ? 4 : 5) : 8) : (D == 128 ? 2 : 4);
   static constexpr int KB = D / 64;                       // 128-byte column blocks per row
   static constexpr int kRegionA = kTileRows * 128;        // one column block of a K tile
   static constexpr int kTileBytes = KB * kRegionA;
@@ -314,7 +350,7 @@ struct Smem {
   static constexpr int kOffBar = kOffQ + kQBytes;         // up to 32 mbarriers
   static constexpr int kOffMisc = kOffBar + 256;          // tmem slot + control words
   static constexpr int kOffRed = kOffMisc + 64;           // [kEpiWarps][kRedStride]
-  static constexpr int kOffMc = kOffRed + kEpiWarps * kRedStride * 4;   // [3][W] chunk maxima
+  static constexpr int kOffMc = kOffRed + R::kEpiWarps * kRedStride * 4;   // [3][W] chunk maxima
   static constexpr int kOffCa = kOffMc + 3 * W * 4;       // [W] a coefficients
   static constexpr int kOffCc = kOffCa + W * 4;           // [kMaxWalk] walk coefficients
   static constexpr int kOffNm = kOffCc + kMaxWalk * 4;    // [W] -max * cl2 of the chunk
@@ -323,12 +359,13 @@ struct Smem {
   static constexpr int kOffMs = kOffMrec + 3 * kMrec * 4; // merge warp scratch [2][W]
   static constexpr int kOffPart = kOffMs + 2 * W * 4;
   // pass-2 partial a per tile, warpgroup and row; the walk term per tile and row
-  static constexpr int kOffCt = kOffPart + kMaxChunkTiles * 4 * kTileRows * 4;
+  static constexpr int kOffCt = kOffPart + R::kMaxChunkTiles * NWG * kTileRows * 4;
   // merge staging: kGroup chunk records as laid out in global memory
   static constexpr int kRecStride = (kRec + 3) / 4 * 4;
-  static constexpr int kOffStage = kOffCt + kMaxChunkTiles * kTileRows * 4;
-  static constexpr int kBytes = kOffStage + kGroup * kRecStride * 4;
-  static constexpr int kAlloc = kBytes + 1024;            // slack for 1024-byte alignment
+  static constexpr int kOffStage = kOffCt + R::kMaxChunkTiles * kTileRows * 4;
+  static constexpr int kBytes = kOffStage + R::kGroup * kRecStride * 4;
+  static constexpr int kTeamBytes = (kBytes + 1023) / 1024 * 1024;   // one team's region
+  static constexpr int kAlloc = R::kTeams * kTeamBytes + 1024;     // + 1024-byte alignment
 };
 
 // The chunk schedule. The chunks of all slices are numbered in slice order (a slice that
@@ -340,13 +377,16 @@ struct Smem {
 // sequence itself, warp-collectively: 32 slices at a time, one per lane, with a warp
 // scan of their chunk counts.
 struct Sched {
+  int cta, ncta;     // this (virtual) CTA and how many there are
   long long first;   // chunk number of the first chunk of slice `base`
   int base;          // first slice of the current batch
   uint32_t mask;     // lanes whose slice has a chunk for this CTA
   int k, T;          // this lane's slice: the chunk index for this CTA, its length
 };
 
-__device__ __forceinline__ void sched_init(Sched& S) {
+__device__ __forceinline__ void sched_init(Sched& S, int cta, int ncta) {
+  S.cta = cta;
+  S.ncta = ncta;
   S.first = 0;
   S.base = -32;
   S.mask = 0;
@@ -374,8 +414,8 @@ __device__ __forceinline__ bool sched_next(const Args& A, Sched& S, int chunk_ro
       if (lane >= o) incl += y;
     }
     const long long f = S.first + (incl - n);
-    int kk = (int)blockIdx.x - (int)(f % gridDim.x);
-    if (kk < 0) kk += (int)gridDim.x;
+    int kk = S.cta - (int)(f % S.ncta);
+    if (kk < 0) kk += S.ncta;
     S.k = kk;
     S.T = t;
     S.mask = __ballot_sync(0xffffffffu, kk < n);
@@ -406,9 +446,9 @@ __device__ __forceinline__ long long global_ns() {
 
 // Phase trace (diagnostics, off unless a buffer is installed): event e of this CTA gets
 // (tag, globaltimer ns); the last three slots hold kernel-level marks.
-__device__ __forceinline__ void trace_ev(const Args& A, int& n, int tag) {
+__device__ __forceinline__ void trace_ev(const Args& A, int cta, int& n, int tag) {
   if (A.trace && n < kTraceEvents - 3) {
-    long long* t = A.trace + ((long long)blockIdx.x * kTraceEvents + n) * 2;
+    long long* t = A.trace + ((long long)cta * kTraceEvents + n) * 2;
     t[0] = tag;
     t[1] = global_ns();
     ++n;
@@ -416,9 +456,9 @@ __device__ __forceinline__ void trace_ev(const Args& A, int& n, int tag) {
 }
 
 // kernel-level marks in the last three trace slots of the CTA: entry, setup done, exit
-__device__ __forceinline__ void trace_mark(const Args& A, int slot, int tag) {
+__device__ __forceinline__ void trace_mark(const Args& A, int cta, int slot, int tag) {
   if (A.trace) {
-    long long* t = A.trace + ((long long)blockIdx.x * kTraceEvents + kTraceEvents - 3 + slot) * 2;
+    long long* t = A.trace + ((long long)cta * kTraceEvents + kTraceEvents - 3 + slot) * 2;
     t[0] = tag;
     t[1] = global_ns();
   }
@@ -450,39 +490,48 @@ __device__ __forceinline__ Chunk make_chunk(const Args& A, int slice, int k, int
   return ch;
 }
 
-// Epilogue state shared by the passes. The W query columns are split over the four
-// warpgroups (warpgroup g owns columns [g W/4, (g+1) W/4)); the four warps of a warpgroup
-// own the 128 rows of a tile (TMEM lanes). The walk rows, the last H <= W/4 columns,
-// belong to warpgroup 3.
-template <int W, int D>
+// Epilogue state shared by the passes. The W query columns are split over the NWG
+// warpgroups (warpgroup g owns columns [g W/NWG, (g+1) W/NWG)); the four warps of a
+// warpgroup own the 128 rows of a tile (TMEM lanes). The walk rows, the last H <= W/NWG
+// columns, belong to the last warpgroup.
+template <int W, int D, int NWG>
 struct Epi {
-  static constexpr int CW = W / 4;
+  static constexpr int CW = W / NWG;
+  static constexpr int kWalkWg = NWG - 1;
+  // tiles whose TMEM loads share one wait, per pass (two measured slower than one: the
+  // passes are bound by arithmetic and barriers, not by the load latency)
+  static constexpr int P1a = 1, P1b = 1, P2 = 1;
   const Args& A;
   uint8_t* sm;
   uint32_t tmem;
   uint32_t buf_cols;
   float cl2;
   int H;
+  int tid;              // thread index within the team
+  int vcta, vgrid;      // this team's place in the chunk schedule
+  int bar_id;           // the team epilogue's named barrier
   int warp, lane, wg, lg, col0;
   int nev = 0;          // trace events written (thread 0)
-  __device__ Epi(const Args& a, uint8_t* s, uint32_t t, uint32_t bc, float c2, int h)
-      : A(a), sm(s), tmem(t), buf_cols(bc), cl2(c2), H(h) {
-    warp = threadIdx.x >> 5;
-    lane = threadIdx.x & 31;
+  __device__ Epi(const Args& a, uint8_t* s, uint32_t t, uint32_t bc, float c2, int h, int ti,
+                 int vc, int vg, int bid)
+      : A(a), sm(s), tmem(t), buf_cols(bc), cl2(c2), H(h), tid(ti), vcta(vc), vgrid(vg),
+        bar_id(bid) {
+    warp = tid >> 5;
+    lane = tid & 31;
     wg = warp >> 2;
     lg = warp & 3;
     col0 = wg * CW;
   }
-  __device__ float* red() { return reinterpret_cast<float*>(sm + Smem<W, D>::kOffRed); }
+  __device__ float* red() { return reinterpret_cast<float*>(sm + Smem<W, D, NWG>::kOffRed); }
   __device__ float* mc(uint32_t b) {
-    return reinterpret_cast<float*>(sm + Smem<W, D>::kOffMc) + b * W;
+    return reinterpret_cast<float*>(sm + Smem<W, D, NWG>::kOffMc) + b * W;
   }
-  __device__ float* ca() { return reinterpret_cast<float*>(sm + Smem<W, D>::kOffCa); }
-  __device__ float* cc() { return reinterpret_cast<float*>(sm + Smem<W, D>::kOffCc); }
-  __device__ float* nm() { return reinterpret_cast<float*>(sm + Smem<W, D>::kOffNm); }
-  __device__ float* recs() { return reinterpret_cast<float*>(sm + Smem<W, D>::kOffRec); }
-  __device__ float* apart() { return reinterpret_cast<float*>(sm + Smem<W, D>::kOffPart); }
-  __device__ float* ctp() { return reinterpret_cast<float*>(sm + Smem<W, D>::kOffCt); }
+  __device__ float* ca() { return reinterpret_cast<float*>(sm + Smem<W, D, NWG>::kOffCa); }
+  __device__ float* cc() { return reinterpret_cast<float*>(sm + Smem<W, D, NWG>::kOffCc); }
+  __device__ float* nm() { return reinterpret_cast<float*>(sm + Smem<W, D, NWG>::kOffNm); }
+  __device__ float* recs() { return reinterpret_cast<float*>(sm + Smem<W, D, NWG>::kOffRec); }
+  __device__ float* apart() { return reinterpret_cast<float*>(sm + Smem<W, D, NWG>::kOffPart); }
+  __device__ float* ctp() { return reinterpret_cast<float*>(sm + Smem<W, D, NWG>::kOffCt); }
   __device__ uint32_t taddr(const Chunk& ch, int t) {
     return tmem + ((uint32_t)(lg * 32) << 16) + ch.b * buf_cols + (uint32_t)(t * W + col0);
   }
@@ -494,82 +543,97 @@ struct Epi {
   // sums and the walk-row Gram; the record goes to global memory.
   template <int HT>
   __device__ void stats(const Chunk& ch) {
-    constexpr int RS = Smem<W, D>::kRedStride;
+    constexpr int RS = Smem<W, D, NWG>::kRedStride;
     float* m = mc(ch.b);
     float mx[CW];
 #pragma unroll
     for (int i = 0; i < CW; ++i) mx[i] = -INFINITY;
-    for (int t = 0; t < ch.ntiles; ++t) {
-      const bool valid = row_valid(ch, t);
-      float v[CW];
-      tmem_ldn<CW>(taddr(ch, t), v);
+    for (int t0 = 0; t0 < ch.ntiles; t0 += P1a) {
+      uint32_t r[P1a][CW];
 #pragma unroll
-      for (int i = 0; i < CW; ++i) mx[i] = fmaxf(mx[i], valid ? v[i] : -INFINITY);
+      for (int u = 0; u < P1a; ++u)
+        if (t0 + u < ch.ntiles) tmem_ld_issue<CW>(taddr(ch, t0 + u), r[u]);
+      tmem_ld_wait();
+#pragma unroll
+      for (int u = 0; u < P1a; ++u) {
+        const bool valid = t0 + u < ch.ntiles && row_valid(ch, t0 + u);
+#pragma unroll
+        for (int i = 0; i < CW; ++i)
+          mx[i] = fmaxf(mx[i], valid ? __uint_as_float(r[u][i]) : -INFINITY);
+      }
     }
-    if (threadIdx.x == 0) trace_ev(A, nev, 10);
+    if (tid == 0) trace_ev(A, vcta, nev, 10);
 #pragma unroll
     for (int i = 0; i < CW; ++i) {
       const float x = warp_max_redux(mx[i]);
       if (lane == 0) red()[warp * RS + col0 + i] = x;
     }
-    epi_sync();
-    if (threadIdx.x < W) {
-      const int col = threadIdx.x, g = col / CW;
+    epi_sync<NWG>(bar_id);
+    if (tid < W) {
+      const int col = tid, g = col / CW;
       float x = red()[(4 * g) * RS + col];
       for (int q = 1; q < 4; ++q) x = fmaxf(x, red()[(4 * g + q) * RS + col]);
       m[col] = x;
       nm()[col] = -x * cl2;
     }
-    epi_sync();
-    if (threadIdx.x == 0) trace_ev(A, nev, 11);
-    float z[CW], gp[kMaxPairs], snm[CW];
+    epi_sync<NWG>(bar_id);
+    if (tid == 0) trace_ev(A, vcta, nev, 11);
+    float z[CW], gp[kMaxPairs];
 #pragma unroll
     for (int i = 0; i < CW; ++i) {
       z[i] = 0.f;
-      snm[i] = nm()[col0 + i];
     }
 #pragma unroll
     for (int i = 0; i < kMaxPairs; ++i) gp[i] = 0.f;
-    const bool walk_wg = (wg == 3);
-    for (int t = 0; t < ch.ntiles; ++t) {
-      const bool valid = row_valid(ch, t);
-      float v[CW];
-      const uint32_t ta = taddr(ch, t);
-      tmem_ldn<CW>(ta, v);
+    const bool walk_wg = (wg == kWalkWg);
+    for (int t0 = 0; t0 < ch.ntiles; t0 += P1b) {
+      uint32_t r[P1b][CW];
 #pragma unroll
-      for (int i = 0; i < CW; ++i) {
-        const float e = valid ? ex2_approx(fmaf(v[i], cl2, snm[i])) : 0.f;
-        v[i] = e;
-        z[i] += e;
-      }
-      tmem_stn<CW>(ta, v);
-      if (walk_wg) {
-        float ew[kMaxWalk];
-        if (HT >= 0) {
+      for (int u = 0; u < P1b; ++u)
+        if (t0 + u < ch.ntiles) tmem_ld_issue<CW>(taddr(ch, t0 + u), r[u]);
+      tmem_ld_wait();
 #pragma unroll
-          for (int tt = 0; tt < kMaxWalk; ++tt) ew[tt] = (tt < HT) ? v[CW - HT + tt] : 0.f;
+      for (int u = 0; u < P1b; ++u) {
+        const int t = t0 + u;
+        if (t >= ch.ntiles) break;
+        const bool valid = row_valid(ch, t);
+        float v[CW];
 #pragma unroll
-          for (int tt = 1; tt < (HT > 0 ? HT : 1); ++tt)
+        for (int i = 0; i < CW; ++i) {
+          const float e =
+              valid ? ex2_approx(fmaf(__uint_as_float(r[u][i]), cl2, nm()[col0 + i])) : 0.f;
+          v[i] = e;
+          z[i] += e;
+        }
+        tmem_stn<CW>(taddr(ch, t), v);
+        if (walk_wg) {
+          float ew[kMaxWalk];
+          if (HT >= 0) {
 #pragma unroll
-            for (int uu = 0; uu < tt; ++uu) gp[pair_index(uu, tt)] += ew[uu] * ew[tt];
-        } else {
+            for (int tt = 0; tt < kMaxWalk; ++tt) ew[tt] = (tt < HT) ? v[CW - HT + tt] : 0.f;
 #pragma unroll
-          for (int tt = 0; tt < kMaxWalk; ++tt) {
-            float x = 0.f;
+            for (int tt = 1; tt < (HT > 0 ? HT : 1); ++tt)
 #pragma unroll
-            for (int i = 0; i < CW; ++i)
-              if (tt < H && i == CW - H + tt) x = v[i];
-            ew[tt] = x;
+              for (int uu = 0; uu < tt; ++uu) gp[pair_index(uu, tt)] += ew[uu] * ew[tt];
+          } else {
+#pragma unroll
+            for (int tt = 0; tt < kMaxWalk; ++tt) {
+              float x = 0.f;
+#pragma unroll
+              for (int i = 0; i < CW; ++i)
+                if (tt < H && i == CW - H + tt) x = v[i];
+              ew[tt] = x;
+            }
+#pragma unroll
+            for (int tt = 1; tt < kMaxWalk; ++tt)
+#pragma unroll
+              for (int uu = 0; uu < tt; ++uu) gp[pair_index(uu, tt)] += ew[uu] * ew[tt];
           }
-#pragma unroll
-          for (int tt = 1; tt < kMaxWalk; ++tt)
-#pragma unroll
-            for (int uu = 0; uu < tt; ++uu) gp[pair_index(uu, tt)] += ew[uu] * ew[tt];
         }
       }
     }
     tmem_st_wait();
-    if (threadIdx.x == 0) trace_ev(A, nev, 12);
+    if (tid == 0) trace_ev(A, vcta, nev, 12);
 #pragma unroll
     for (int i = 0; i < CW; ++i) {
       const float x = warp_sum(z[i]);
@@ -583,49 +647,45 @@ struct Epi {
         if (lane == 0) red()[warp * RS + W + i] = x;
       }
     }
-    epi_sync();
+    epi_sync<NWG>(bar_id);
     float* rec = A.partial + ((long long)ch.slice * A.maxc + ch.k) * A.stride;
-    if (threadIdx.x < W) {
-      const int col = threadIdx.x, g = col / CW;
+    if (tid < W) {
+      const int col = tid, g = col / CW;
       float x = 0.f;
       for (int q = 0; q < 4; ++q) x += red()[(4 * g + q) * RS + col];
       rec[col] = m[col];                  // chunk max (raw)
       rec[W + col] = x;                   // sum relative to it
-    } else if (threadIdx.x < W + kMaxPairs) {
-      const int k = threadIdx.x - W;
+    } else if (tid < W + kMaxPairs) {
+      const int k = tid - W;
       float x = 0.f;
-      for (int q = 0; q < 4; ++q) x += red()[(12 + q) * RS + W + k];
+      for (int q = 0; q < 4; ++q) x += red()[(4 * kWalkWg + q) * RS + W + k];
       rec[2 * W + k] = x;                 // Gram entry
     }
   }
 
   // Publish the chunk's record: count it in for its slice (thread 0, after a fence).
-  __device__ void publish(const Chunk& ch, bool ok) {
-    using S = Smem<W, D>;
+  // Hand the chunk's record to the publisher warp: each epilogue warp arrives once its
+  // stores are issued (the arrive orders them before the publisher's fence).
+  __device__ void publish(const Chunk& ch, bool ok, uint64_t* bar_pub) {
+    using S = Smem<W, D, NWG>;
     int* ctl = reinterpret_cast<int*>(sm + S::kOffMisc + 16);
-    epi_sync();
-    if (threadIdx.x == 0) {
-      if (!ok) {
-        ctl[1] = 1;
-      } else {
-        __threadfence();
-        atomicAdd(&A.arrive[ch.slice], 1);
-      }
-    }
+    if (!ok && tid == 0) ctl[1] = 1;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar_pub[ch.b]);
   }
 
   // Wait for the slice, merge, then a, c~, w and the order key of every row.
   template <int HT>
   __device__ bool emit(const Chunk& ch) {
-    using S = Smem<W, D>;
+    using S = Smem<W, D, NWG>;
     int* ctl = reinterpret_cast<int*>(sm + S::kOffMisc + 16);
     const nx_cache& c = A.c;
     const nx_params& p = A.p;
-    // rows this thread finalizes: tiles t = wg, wg + 4 (at most two); positions first
+    // rows this thread finalizes: tiles t = wg, wg + NWG (at most two); positions first
     int32_t posv[2];
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-      const int t = wg + 4 * r;
+      const int t = wg + NWG * r;
       const int j = ch.j0 + t * kTileRows + lg * 32 + lane;
       posv[r] = (t < ch.ntiles && j < ch.T && (A.out.flags & kEmitKeys))
                     ? __ldg(&c.pos[row_of(c, ch.l, ch.s, ch.h, j)]) : 0;
@@ -634,68 +694,82 @@ struct Epi {
     // waits (the abort flag may be set by other warps at any time) and everyone acts on
     // its snapshot after the barrier
     uint64_t* bar_mfull = reinterpret_cast<uint64_t*>(sm + S::kOffBar) + 2 * S::kStages + 8;
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
       if (!ctl[1] && !mbar_wait(&bar_mfull[ch.b], ch.use & 1, A.dev_status)) ctl[1] = 1;
       ctl[2] = ctl[1];
     }
-    epi_sync();
-    if (threadIdx.x == 0) trace_ev(A, nev, 5 + 1000 * (ch.slice + 1));
+    epi_sync<NWG>(bar_id);
+    if (tid == 0) trace_ev(A, vcta, nev, 5 + 1000 * (ch.slice + 1));
     if (ctl[2]) return false;
     const float* mr = reinterpret_cast<const float*>(sm + S::kOffMrec) + ch.b * S::kMrec;
     const float* m = mc(ch.b);
-    if (threadIdx.x < W) {
-      const int w = threadIdx.x;
+    if (tid < W) {
+      const int w = tid;
       // fold this chunk's max shift into the slice's per-row weights
       const float shift = exp2f((m[w] - mr[w]) * cl2);
       ca()[w] = shift / ((float)W * mr[W + w]);
       if (w >= W - H) cc()[w - (W - H)] = mr[2 * W + (w - (W - H))] * shift;
     }
-    if (ch.k == 0 && (A.out.flags & kEmitStats) && threadIdx.x < W) {
-      const int w = threadIdx.x;
+    if (ch.k == 0 && (A.out.flags & kEmitStats) && tid < W) {
+      const int w = tid;
       A.out.row_stats[((long long)ch.slice * W + w) * 2] = mr[w] * rsqrtf((float)D);
       A.out.row_stats[((long long)ch.slice * W + w) * 2 + 1] = mr[W + w];
     }
-    epi_sync();
-    if (threadIdx.x == 0) trace_ev(A, nev, 6);
+    epi_sync<NWG>(bar_id);
+    if (tid == 0) trace_ev(A, vcta, nev, 6);
     // partial sums over this warpgroup's columns for every tile, one barrier, then each
     // warpgroup finalizes a quarter of the tiles
-    float sca[CW], scc[kMaxWalk];
-#pragma unroll
-    for (int i = 0; i < CW; ++i) sca[i] = ca()[col0 + i];
+    float scc[kMaxWalk];
 #pragma unroll
     for (int tt = 0; tt < kMaxWalk; ++tt) scc[tt] = cc()[tt];
     const int row = lg * 32 + lane;
-    for (int t = 0; t < ch.ntiles; ++t) {
-      float v[CW];
-      tmem_ldn<CW>(taddr(ch, t), v);
-      float a4[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int t0 = 0; t0 < ch.ntiles; t0 += P2) {
+      uint32_t r[P2][CW];
 #pragma unroll
-      for (int i = 0; i < CW; ++i) a4[i & 3] = fmaf(v[i], sca[i], a4[i & 3]);
-      apart()[(t * 4 + wg) * kTileRows + row] = (a4[0] + a4[1]) + (a4[2] + a4[3]);
-      if (wg == 3) {
-        float ct = 0.f;
-        if (HT >= 0) {
+      for (int u = 0; u < P2; ++u)
+        if (t0 + u < ch.ntiles) tmem_ld_issue<CW>(taddr(ch, t0 + u), r[u]);
+      tmem_ld_wait();
 #pragma unroll
-          for (int tt = 0; tt < (HT > 0 ? HT : 0); ++tt) ct = fmaf(v[CW - HT + tt], scc[tt], ct);
-        } else {
+      for (int u = 0; u < P2; ++u) {
+        const int t = t0 + u;
+        if (t >= ch.ntiles) break;
+        float v[CW];
 #pragma unroll
-          for (int i = 0; i < CW; ++i)
-            if (i >= CW - H) ct = fmaf(v[i], scc[(i - (CW - H)) & (kMaxWalk - 1)], ct);
+        for (int i = 0; i < CW; ++i) v[i] = __uint_as_float(r[u][i]);
+        float a4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < CW; ++i) a4[i & 3] = fmaf(v[i], ca()[col0 + i], a4[i & 3]);
+        apart()[(t * NWG + wg) * kTileRows + row] = (a4[0] + a4[1]) + (a4[2] + a4[3]);
+        if (wg == kWalkWg) {
+          float ct = 0.f;
+          if (HT >= 0) {
+#pragma unroll
+            for (int tt = 0; tt < (HT > 0 ? HT : 0); ++tt)
+              ct = fmaf(v[CW - HT + tt], scc[tt], ct);
+          } else {
+#pragma unroll
+            for (int i = 0; i < CW; ++i)
+              if (i >= CW - H) ct = fmaf(v[i], scc[(i - (CW - H)) & (kMaxWalk - 1)], ct);
+          }
+          ctp()[t * kTileRows + row] = ct;
         }
-        ctp()[t * kTileRows + row] = ct;
       }
     }
-    epi_sync();
+    epi_sync<NWG>(bar_id);
     const uint32_t head_id = (uint32_t)((p.layer_id_base + ch.l) * c.kv_heads + ch.h);
     const uint32_t seq_id = (uint32_t)(p.seq_id_base + ch.s);
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-      const int t = wg + 4 * r;
+      const int t = wg + NWG * r;
       if (t >= ch.ntiles) break;
       const int j = ch.j0 + t * kTileRows + row;
       if (j >= ch.T) continue;
-      const float* ap = apart() + t * 4 * kTileRows + row;
-      const float a = (ap[0] + ap[kTileRows]) + (ap[2 * kTileRows] + ap[3 * kTileRows]);
+      const float* ap = apart() + t * NWG * kTileRows + row;
+      float a;
+      if (NWG == 4)
+        a = (ap[0] + ap[kTileRows]) + (ap[2 * kTileRows] + ap[3 * kTileRows]);
+      else
+        a = ap[0] + ap[kTileRows];
       const float ct = ctp()[t * kTileRows + row];
       const float sj = a + p.lambda * ct;
       const float ramp = (ch.T > 1) ? (float)j / (float)(ch.T - 1) : 0.f;
@@ -717,41 +791,42 @@ struct Epi {
   // The epilogue loop, software-pipelined when TMEM holds two or more chunks: chunk c+1's
   // statistics are computed and published before chunk c waits for its slice.
   template <int HT>
-  __device__ void run(uint64_t* bar_tfull, uint64_t* bar_tempty, int chunk_rows, int nbuf) {
-    using S = Smem<W, D>;
+  __device__ void run(uint64_t* bar_tfull, uint64_t* bar_tempty, uint64_t* bar_pub,
+                      int chunk_rows, int nbuf) {
+    using S = Smem<W, D, NWG>;
     int* ctl = reinterpret_cast<int*>(sm + S::kOffMisc + 16);
     Chunk prev;
     bool have_prev = false;
     uint32_t cnt = 0;
     auto finish = [&](const Chunk& ch) -> bool {
-      if (threadIdx.x == 0) trace_ev(A, nev, 3 + 1000 * (ch.slice + 1));
+      if (tid == 0) trace_ev(A, vcta, nev, 3 + 1000 * (ch.slice + 1));
       const bool ok = emit<HT>(ch);
       tc_fence_before();
-      epi_sync();
-      if (threadIdx.x == 0) {
-        trace_ev(A, nev, 4);
+      epi_sync<NWG>(bar_id);
+      if (tid == 0) {
+        trace_ev(A, vcta, nev, 4);
         mbar_arrive(&bar_tempty[ch.b]);
         if (!ok) ctl[1] = 1;
       }
       return ok;
     };
     Sched sc;
-    sched_init(sc);
+    sched_init(sc, vcta, vgrid);
     int sl, kq, Tq;
     for (; sched_next(A, sc, chunk_rows, sl, kq, Tq); ++cnt) {
-      if (threadIdx.x == 0) ctl[3] = ctl[1];   // one snapshot of the abort flag for all
-      epi_sync();
+      if (tid == 0) ctl[3] = ctl[1];   // one snapshot of the abort flag for all
+      epi_sync<NWG>(bar_id);
       if (ctl[3]) break;
       const Chunk ch = make_chunk(A, sl, kq, Tq, chunk_rows, cnt, nbuf);
-      if (threadIdx.x == 0) trace_ev(A, nev, 100 + ch.k);
-      if (threadIdx.x == 0) ctl[2] = mbar_wait(&bar_tfull[ch.b], ch.use & 1, A.dev_status) ? 1 : 0;
-      epi_sync();
+      if (tid == 0) trace_ev(A, vcta, nev, 100 + ch.k);
+      if (tid == 0) ctl[2] = mbar_wait(&bar_tfull[ch.b], ch.use & 1, A.dev_status) ? 1 : 0;
+      epi_sync<NWG>(bar_id);
       const bool ok = ctl[2] != 0;
       tc_fence_after();
-      if (threadIdx.x == 0) trace_ev(A, nev, 1);
+      if (tid == 0) trace_ev(A, vcta, nev, 1);
       if (ok) stats<HT>(ch);
-      if (threadIdx.x == 0) trace_ev(A, nev, 2 + 1000 * (ch.slice + 1));
-      publish(ch, ok);
+      if (tid == 0) trace_ev(A, vcta, nev, 2 + 1000 * (ch.slice + 1));
+      publish(ch, ok, bar_pub);
       if (!ok) break;
       if (nbuf == 1) {
         if (!finish(ch)) break;
@@ -761,8 +836,8 @@ struct Epi {
         have_prev = true;
       }
     }
-    if (threadIdx.x == 0) ctl[3] = ctl[1];
-    epi_sync();
+    if (tid == 0) ctl[3] = ctl[1];
+    epi_sync<NWG>(bar_id);
     if (nbuf != 1 && have_prev && !ctl[3]) finish(prev);
   }
 };
@@ -772,11 +847,11 @@ struct Epi {
 // the slice's chunk records into shared memory (one bulk copy per kGroup records) and
 // merge them with an online rescale across batches: per window row the maximum and the
 // normaliser, and the walk coefficients gamma_t / (sum gamma * Z_t) of Eq. (4).
-template <int W, int D>
+template <int W, int D, int NWG>
 __device__ void merge_warp(const Args& A, uint8_t* sm, int chunk_rows, int nbuf, float cl2,
                            uint64_t* bar_tempty, uint64_t* bar_mfull, uint64_t* bar_htx,
-                           volatile int* abort_flag) {
-  using S = Smem<W, D>;
+                           volatile int* abort_flag, int vcta, int vgrid) {
+  using S = Smem<W, D, NWG>;
   constexpr int QW = (W + 31) / 32;       // columns per lane
   const int lane = threadIdx.x & 31;
   const int H = A.p.walk_len;
@@ -784,7 +859,7 @@ __device__ void merge_warp(const Args& A, uint8_t* sm, int chunk_rows, int nbuf,
   float* ms = reinterpret_cast<float*>(sm + S::kOffMs);     // [0]: maxima, [1]: normalisers
   uint32_t cnt = 0, htx = 0;
   Sched sc;
-  sched_init(sc);
+  sched_init(sc, vcta, vgrid);
   int sl, kq, Tq;
   for (; !warp_flag(abort_flag) && sched_next(A, sc, chunk_rows, sl, kq, Tq); ++cnt) {
     const Chunk ch = make_chunk(A, sl, kq, Tq, chunk_rows, cnt, nbuf);
@@ -811,8 +886,9 @@ __device__ void merge_warp(const Args& A, uint8_t* sm, int chunk_rows, int nbuf,
     const bool gact = lane < kMaxPairs && gt < H;
     const int wp = W - H + gu, wq = W - H + gt;
     const float* src = A.partial + (long long)ch.slice * A.maxc * A.stride;
-    for (int b0 = 0; b0 < ch.nchunks && ok; b0 += kGroup) {
-      const int n = min(kGroup, ch.nchunks - b0);
+    constexpr int NG = Roles<NWG>::kGroup;
+    for (int b0 = 0; b0 < ch.nchunks && ok; b0 += NG) {
+      const int n = min(NG, ch.nchunks - b0);
       if (lane == 0) {
         const uint32_t bytes = (uint32_t)(n * A.stride * 4);
         mbar_expect_tx(bar_htx, bytes);
@@ -885,15 +961,47 @@ __device__ void merge_warp(const Args& A, uint8_t* sm, int chunk_rows, int nbuf,
   }
 }
 
-// 19 warps per CTA: one SM sub-partition holds 5 of them, so the 16K-register share of a
-// sub-partition caps a thread at about 100 registers.
-template <int W, int D>
-__global__ void __launch_bounds__(kThreads, 1)
+// The publisher warp: once the epilogue warps have stored a chunk's record, make it
+// visible device-wide and count it in for its slice (the fence stays off the epilogue's
+// path).
+__device__ void publish_warp(const Args& A, int chunk_rows, int nbuf, uint64_t* bar_pub,
+                             volatile int* abort_flag, int vcta, int vgrid) {
+  const int lane = threadIdx.x & 31;
+  Sched sc;
+  sched_init(sc, vcta, vgrid);
+  int sl, kq, Tq;
+  for (uint32_t cnt = 0; sched_next(A, sc, chunk_rows, sl, kq, Tq); ++cnt) {
+    const uint32_t b = cnt % nbuf, use = cnt / nbuf;
+    int ok = 1;
+    if (lane == 0) {
+      ok = mbar_wait(&bar_pub[b], use & 1, A.dev_status) && !*abort_flag;
+      if (ok) {
+        __threadfence();
+        atomicAdd(&A.arrive[sl], 1);
+      }
+    }
+    if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+  }
+}
+
+// A CTA's warps are dealt round-robin to the SM's four sub-partitions, each with 16K
+// registers: with NWG = 4 (20 warps, one CTA per SM) a sub-partition holds 5 warps, which
+// caps a thread at 96 registers; with NWG = 2 (12 warps, two CTAs per SM) it holds 6,
+// which caps a thread at 80.
+template <int W, int D, int NWG>
+__global__ void __launch_bounds__(Roles<NWG>::kBlockThreads, 1)
 score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
-  using S = Smem<W, D>;
+  using S = Smem<W, D, NWG>;
+  using R = Roles<NWG>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~uintptr_t(1023));
+  uint8_t* sm0 = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                            ~uintptr_t(1023));
+  // this thread's team: its shared-memory region, TMEM share and place in the schedule
+  const int team = (int)threadIdx.x / R::kThreads;
+  const int tid = (int)threadIdx.x - team * R::kThreads;
+  uint8_t* sm = sm0 + team * S::kTeamBytes;
+  const int vcta = (int)blockIdx.x * R::kTeams + team;
+  const int vgrid = (int)gridDim.x * R::kTeams;
   uint64_t* bar_full = reinterpret_cast<uint64_t*>(sm + S::kOffBar);   // [S::kStages]
   uint64_t* bar_empty = bar_full + S::kStages;                           // [S::kStages]
   uint64_t* bar_tfull = bar_empty + S::kStages;                          // [3] TMEM buffer ready
@@ -902,19 +1010,21 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
   uint64_t* bar_qempty = bar_qfull + 1;
   uint64_t* bar_mfull = bar_full + 2 * S::kStages + 8;                 // [3] merged stats ready
   uint64_t* bar_htx = bar_mfull + 3;                                  // merge warp's copies
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S::kOffMisc);
-  int* ctl = reinterpret_cast<int*>(sm + S::kOffMisc + 16);   // [0] merge role, [1] abort
+  uint64_t* bar_pub = bar_htx + 1;                                    // [3] records stored
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm0 + S::kOffMisc);   // team 0's
+  int* ctl = reinterpret_cast<int*>(sm + S::kOffMisc + 16);   // [1] abort, [2-3] snapshots
 
   const nx_cache& c = A.c;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = tid >> 5, lane = tid & 31;
   const float cl2 = kLog2e * rsqrtf((float)D);   // raw accumulator -> log2 units
   constexpr uint32_t kIdesc = idesc_bf16<W>();
   const int chunk_rows = A.tiles_per_chunk * kTileRows;
   const int nbuf = A.nbuf;
-  const uint32_t buf_cols = (A.tmem_cols / (uint32_t)nbuf / W) * W;
+  const uint32_t team_cols = A.tmem_cols / R::kTeams;
+  const uint32_t buf_cols = (team_cols / (uint32_t)nbuf / W) * W;
 
-  if (threadIdx.x == 0) {
-    trace_mark(A, 0, 7);
+  if (tid == 0) {
+    trace_mark(A, vcta, 0, 7);
     for (int i = 0; i < S::kStages; ++i) {
       mbar_init(&bar_full[i], 1);
       mbar_init(&bar_empty[i], 1);
@@ -927,6 +1037,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
     mbar_init(bar_qempty, 1);
     for (int i = 0; i < 3; ++i) mbar_init(&bar_mfull[i], 1);
     mbar_init(bar_htx, 1);
+    for (int i = 0; i < 3; ++i) mbar_init(&bar_pub[i], R::kEpiWarps);
     ctl[0] = 0;
     ctl[1] = 0;
     ctl[2] = 0;
@@ -934,7 +1045,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
   }
-  if (warp == kMmaWarp) {
+  if (team == 0 && warp == R::kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
                  "r"(A.tmem_cols));
@@ -943,16 +1054,16 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem = *tmem_slot + (uint32_t)team * team_cols;   // column offset
   volatile int* abort_flag = ctl + 1;
-  if (threadIdx.x == 0) trace_mark(A, 1, 9);
+  if (tid == 0) trace_mark(A, vcta, 1, 9);
 
-  if (warp == kProducerWarp) {
+  if (warp == R::kProducerWarp) {
     // =================== TMA producer: query images and K tiles ===================
     uint32_t u = 0, qn = 0;
     int prev_slice = -1;
     Sched sc;
-    sched_init(sc);
+    sched_init(sc, vcta, vgrid);
     int slice, k, T;
     while (!warp_flag(abort_flag) && sched_next(A, sc, chunk_rows, slice, k, T)) {
       int fail = 0;
@@ -999,13 +1110,13 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
       }
       if (__shfl_sync(0xffffffffu, fail, 0)) break;
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == R::kMmaWarp) {
     // =================== MMA issuer ===================
     uint32_t u = 0, qn = 0, cc = 0;
     int prev_slice = -1;
     const uint32_t qa = smem_u32(sm + S::kOffQ);
     Sched sc;
-    sched_init(sc);
+    sched_init(sc, vcta, vgrid);
     int slice, k, T;
     for (; !warp_flag(abort_flag) && sched_next(A, sc, chunk_rows, slice, k, T); ++cc) {
       int fail = 0;
@@ -1047,33 +1158,38 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
       }
       if (__shfl_sync(0xffffffffu, fail, 0)) break;
     }
-  } else if (warp == kMergeWarp) {
+  } else if (warp == R::kMergeWarp) {
     // =================== slice merge ===================
-    merge_warp<W, D>(A, sm, chunk_rows, nbuf, cl2, bar_tempty, bar_mfull, bar_htx, abort_flag);
+    merge_warp<W, D, NWG>(A, sm, chunk_rows, nbuf, cl2, bar_tempty, bar_mfull, bar_htx,
+                          abort_flag, vcta, vgrid);
+  } else if (warp == R::kPublishWarp) {
+    // =================== record publisher ===================
+    publish_warp(A, chunk_rows, nbuf, bar_pub, abort_flag, vcta, vgrid);
   } else {
-    // =================== epilogue: warps 0-15 ===================
-    Epi<W, D> epi(A, sm, tmem, buf_cols, cl2, A.p.walk_len);
+    // =================== epilogue: warps [0, 4 NWG) ===================
+    Epi<W, D, NWG> epi(A, sm, tmem, buf_cols, cl2, A.p.walk_len, tid, vcta, vgrid, 1 + team);
     switch (A.p.walk_len) {
-      case 3: epi.template run<3>(bar_tfull, bar_tempty, chunk_rows, nbuf); break;
-      case 5: epi.template run<5>(bar_tfull, bar_tempty, chunk_rows, nbuf); break;
-      default: epi.template run<-1>(bar_tfull, bar_tempty, chunk_rows, nbuf); break;
+      case 3: epi.template run<3>(bar_tfull, bar_tempty, bar_pub, chunk_rows, nbuf); break;
+      case 5: epi.template run<5>(bar_tfull, bar_tempty, bar_pub, chunk_rows, nbuf); break;
+      default: epi.template run<-1>(bar_tfull, bar_tempty, bar_pub, chunk_rows, nbuf); break;
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (team == 0 && warp == R::kMmaWarp) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(*tmem_slot),
                  "r"(A.tmem_cols));
   }
-  if (threadIdx.x == 0) trace_mark(A, 2, 8);
+  if (tid == 0) trace_mark(A, vcta, 2, 8);
 }
 
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 long long* g_trace = nullptr;     // installed by nexus_debug_set_trace
+int g_layout = 0;                 // pipelines per CTA asked for (0: automatic)
 thread_local int32_t g_last_cfg[8];
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1091,11 +1207,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-template <int W, int D>
+template <int W, int D, int NWG>
 cudaError_t launch_t(const nx_cache& c, const nx_params& p, const void* q, const WsLayout& L,
                      char* ws, const ScoreOut& out, int32_t* dev_status, cudaStream_t st,
                      int* launches, bool* used) {
-  using S = Smem<W, D>;
+  using S = Smem<W, D, NWG>;
+  using R = Roles<NWG>;
   *used = false;
   for (int i = 0; i < 8; ++i) g_last_cfg[i] = 0;
   auto fn = encode_fn();
@@ -1122,25 +1239,30 @@ cudaError_t launch_t(const nx_cache& c, const nx_params& p, const void* q, const
   static bool attr_set[64] = {};
   if (dev < 0 || dev >= 64) return cudaSuccess;
   if (!attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(score_tc_kernel<W, D>,
+    cudaError_t e = cudaFuncSetAttribute(score_tc_kernel<W, D, NWG>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, S::kAlloc);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(score_tc_kernel<W, D>,
+    e = cudaFuncSetAttribute(score_tc_kernel<W, D, NWG>,
                              cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_api, score_tc_kernel<W, D>, kThreads,
-                                                S::kAlloc);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_api, score_tc_kernel<W, D, NWG>,
+                                                R::kBlockThreads, S::kAlloc);
+  if (per_sm_api < 1) {
+    g_last_cfg[0] = -6;
+    g_last_cfg[1] = per_sm_api;
+    return cudaSuccess;
+  }
   const long long slices = L.slices;
   const long long cap_tiles = (c.capacity + kTileRows - 1) / kTileRows;
 
-  // One CTA per SM with all 512 TMEM columns (its 8 epilogue warps hide latency).
-  for (int per_sm = 1; per_sm >= 1; --per_sm) {
-    const uint32_t tmem_cols = 512u;
-    const long long grid_max = (long long)sms * per_sm;
+  {
+    const int per_sm = 1;
+    const uint32_t tmem_cols = R::kTmemCols;                     // one team's share
+    const long long grid_max = (long long)sms * R::kTeams;       // teams in the schedule
     // Chunk size and grid: every slice's chunks must be co-resident (the slice barrier),
     // and a round of the grid should hold whole slices (a slice split across two rounds
     // makes its first chunks wait a whole round). Among chunk sizes up to what a TMEM
@@ -1149,31 +1271,43 @@ cudaError_t launch_t(const nx_cache& c, const nx_params& p, const void* q, const
     int nbuf = 0, tpc = 0, maxc = 0;
     long long grid_sel = 0, best = -1;
     for (int nb = 3; nb >= 1; --nb) {
-      const int max_tiles = min(kMaxChunkTiles, (int)(tmem_cols / nb / W));
+      const int max_tiles = min(R::kMaxChunkTiles, (int)(tmem_cols / nb / W));
       for (int t = 1; t <= max_tiles; ++t) {
         const int mc = (int)((cap_tiles + t - 1) / t);
-        if (mc > grid_max || mc > kGroup * kMaxBatches) continue;
-        const long long per = grid_max / mc;                 // whole slices per round
-        const long long rounds = (slices + per - 1) / per;
-        // deeper TMEM buffering overlaps more; ties go to fewer rounds
-        const int depth_cost = nb == 3 ? 20 : (nb == 2 ? 22 : 30);
-        long long cost = (rounds * t * depth_cost) * 4096 + rounds;
+        if (mc > grid_max || mc > kMaxChunksPerSlice) continue;
+        long long cost, gsel;
+        if (R::kTeams == 1) {
+          const long long per = grid_max / mc;                 // whole slices per round
+          const long long rounds = (slices + per - 1) / per;
+          // deeper TMEM buffering overlaps more; ties go to fewer rounds
+          const int depth_cost = nb == 3 ? 20 : (nb == 2 ? 22 : 30);
+          cost = (rounds * t * depth_cost) * 4096 + rounds;
+          gsel = per * mc;
+        } else {
+          // two pipelines per CTA overlap one another, so slices need not align with
+          // rounds: all pipelines take part, and a chunk costs its tiles plus about four
+          // tiles' worth of fixed latency; at least two TMEM buffers
+          if (nb < 2) continue;
+          const long long rounds = (slices * mc + grid_max - 1) / grid_max;
+          cost = (rounds * (t + 4)) * 4 + (3 - nb);
+          gsel = grid_max;
+        }
         if (best < 0 || cost < best) {
           best = cost;
           nbuf = nb;
           tpc = t;
           maxc = mc;
-          grid_sel = per * mc;
+          grid_sel = gsel;
         }
       }
     }
-    if (!nbuf) { g_last_cfg[0] = -4; continue; }
+    if (!nbuf) { g_last_cfg[0] = -4; return cudaSuccess; }
     Args a;
     a.c = c;
     a.p = p;
     (void)q;
     a.qimg = reinterpret_cast<const unsigned char*>(ws + L.qbar);
-    a.tmem_cols = tmem_cols;
+    a.tmem_cols = R::kTeams * tmem_cols;                        // the whole allocation
     a.partial = reinterpret_cast<float*>(ws + L.stats);
     a.arrive = reinterpret_cast<int*>(ws + L.barriers);
     a.newlen = reinterpret_cast<const int32_t*>(ws + L.newlen);
@@ -1186,11 +1320,12 @@ cudaError_t launch_t(const nx_cache& c, const nx_params& p, const void* q, const
     a.total_ids = slices * maxc;
     a.slices = (int)slices;
     a.trace = g_trace;
-    const long long grid = a.total_ids < grid_sel ? a.total_ids : grid_sel;
+    const long long vgrid = a.total_ids < grid_sel ? a.total_ids : grid_sel;
+    const long long grid = (vgrid + R::kTeams - 1) / R::kTeams;  // CTAs of kTeams teams
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(R::kBlockThreads);
     cfg.dynamicSmemBytes = S::kAlloc;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -1198,15 +1333,16 @@ cudaError_t launch_t(const nx_cache& c, const nx_params& p, const void* q, const
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, score_tc_kernel<W, D>, map, a);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, score_tc_kernel<W, D, NWG>, map, a);
     if (e == cudaErrorCooperativeLaunchTooLarge) {
       (void)cudaGetLastError();
       g_last_cfg[0] = -5;
       g_last_cfg[1] = per_sm_api;
-      continue;
+      return cudaSuccess;
     }
     if (e != cudaSuccess) return e;
-    g_last_cfg[0] = per_sm;
+    g_last_cfg[0] = R::kTeams;
+    (void)per_sm;
     g_last_cfg[1] = per_sm_api;
     g_last_cfg[2] = (int32_t)grid;
     g_last_cfg[3] = tpc;
@@ -1224,6 +1360,7 @@ cudaError_t launch_t(const nx_cache& c, const nx_params& p, const void* q, const
 }  // namespace tc
 
 void tc_set_trace(long long* buf) { tc::g_trace = buf; }
+void tc_set_layout(int teams) { tc::g_layout = teams; }
 void tc_last_config(int32_t* out) {
   for (int i = 0; i < 8; ++i) out[i] = tc::g_last_cfg[i];
 }
@@ -1243,17 +1380,27 @@ cudaError_t launch_score_tc(const nx_cache& c, const nx_params& p, const void* q
   *used = false;
   if (!tc_supported(c, p)) return cudaSuccess;
   const bool d128 = c.head_dim == 128;
-  switch (p.window) {
-    case 16:
-      return d128 ? tc::launch_t<16, 128>(c, p, q, L, ws, out, dev_status, st, launches, used)
-                  : tc::launch_t<16, 64>(c, p, q, L, ws, out, dev_status, st, launches, used);
-    case 32:
-      return d128 ? tc::launch_t<32, 128>(c, p, q, L, ws, out, dev_status, st, launches, used)
-                  : tc::launch_t<32, 64>(c, p, q, L, ws, out, dev_status, st, launches, used);
-    default:
-      return d128 ? tc::launch_t<64, 128>(c, p, q, L, ws, out, dev_status, st, launches, used)
-                  : tc::launch_t<64, 64>(c, p, q, L, ws, out, dev_status, st, launches, used);
+#define NX_TC_LAUNCH(WW, DD, NN) \
+  tc::launch_t<WW, DD, NN>(c, p, q, L, ws, out, dev_status, st, launches, used)
+  // Windows of up to 32 rows may take two pipelines per CTA. Automatic choice: two for large
+  // paged caches (one TMA copy per page: two producers keep more of them in flight), one
+  // otherwise (measured faster for contiguous caches); a layout that cannot run falls back.
+  const long long rows_all = (long long)c.layers * c.seqs * c.kv_heads * c.capacity;
+  int sms = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const bool big = rows_all >= 8LL * 512 * (sms > 0 ? sms : 1) && c.page_size > 0;
+  if (p.window <= 32 && (tc::g_layout == 2 || (tc::g_layout == 0 && big))) {
+    cudaError_t e = p.window == 16 ? (d128 ? NX_TC_LAUNCH(16, 128, 2) : NX_TC_LAUNCH(16, 64, 2))
+                                   : (d128 ? NX_TC_LAUNCH(32, 128, 2) : NX_TC_LAUNCH(32, 64, 2));
+    if (e != cudaSuccess || *used || tc::g_layout == 2) return e;
   }
+  switch (p.window) {
+    case 16: return d128 ? NX_TC_LAUNCH(16, 128, 4) : NX_TC_LAUNCH(16, 64, 4);
+    case 32: return d128 ? NX_TC_LAUNCH(32, 128, 4) : NX_TC_LAUNCH(32, 64, 4);
+    default: return d128 ? NX_TC_LAUNCH(64, 128, 4) : NX_TC_LAUNCH(64, 64, 4);
+  }
+#undef NX_TC_LAUNCH
 }
 
 }  // namespace nx

@@ -28,7 +28,7 @@ SYMBOLS = ("nexus_workspace_bytes", "nexus_direct_scores", "nexus_walk",
            "nexus_reservoir_select", "kv_compact", "nexus_evict_step", "nx_status_string",
            "nexus_last_launch_count", "nexus_debug_compact", "nexus_last_launch_name",
            "nexus_profile_next_call", "nexus_debug_force_simt", "nexus_debug_set_trace",
-           "nexus_debug_scorer_config")
+           "nexus_debug_scorer_config", "nexus_debug_scorer_layout", "kv_compact_noalloc")
 
 
 class NexusError(RuntimeError):
@@ -89,6 +89,8 @@ def load(path: str = LIB_PATH):
             lib.nexus_profile_next_call.restype = None
             lib.nexus_debug_force_simt.argtypes = [ctypes.c_int32]
             lib.nexus_debug_force_simt.restype = None
+            lib.nexus_debug_scorer_layout.argtypes = [ctypes.c_int32]
+            lib.nexus_debug_scorer_layout.restype = None
             lib.nexus_debug_set_trace.argtypes = [ctypes.c_void_p]
             lib.nexus_debug_set_trace.restype = None
             lib.nexus_debug_scorer_config.argtypes = [ctypes.c_void_p]
@@ -102,11 +104,16 @@ def force_simt(on: bool) -> None:
     load().nexus_debug_force_simt(1 if on else 0)
 
 
+def scorer_layout(teams: int) -> None:
+    """Tensor-core scorer layout: 2 or 1 pipelines per CTA, 0 for the automatic choice."""
+    load().nexus_debug_scorer_layout(int(teams))
+
+
 def scorer_config() -> dict:
     """Configuration of the last tensor-core scorer launch made from this thread."""
     out = (ctypes.c_int32 * 8)()
     load().nexus_debug_scorer_config(out)
-    keys = ("ctas_per_sm", "occupancy_api", "grid", "tiles_per_chunk", "tmem_buffers",
+    keys = ("teams_per_cta", "occupancy_api", "grid", "tiles_per_chunk", "tmem_buffers",
             "chunks_per_slice", "tmem_cols", "smem_bytes")
     return dict(zip(keys, list(out)))
 

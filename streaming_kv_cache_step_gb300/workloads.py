@@ -544,12 +544,19 @@ def streaming_paged(n_seqs: int = 256) -> Workload:
                     query_gain=2.0, seed=DATA_SEED_BASE + 4)
 
 
+def batch16_1layer() -> Workload:
+    """One layer of the 16-sequence batch (128 slices, 1 GiB of keys): a profiling case
+    larger than L2 that a counter capture replays quickly."""
+    return dataclasses.replace(batch16_32layers(), name="batch16_1layer", layers=1)
+
+
 WORKLOADS = {
     "tiny": tiny,
     "llama3_8b_layer": llama3_8b_layer,
     "batch16_32layers": batch16_32layers,
     "long_context": long_context,
     "streaming_paged": streaming_paged,
+    "batch16_1layer": batch16_1layer,
 }
 
 

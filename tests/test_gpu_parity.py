@@ -33,6 +33,30 @@ def _cases():
 
 CASES = _cases()
 
+# tensor-core scorer layouts: 0 the automatic choice (one pipeline per CTA at these sizes),
+# 2 two pipelines per CTA (windows of up to 32 rows, bf16)
+LAYOUTS = [0, 2]
+
+
+@pytest.fixture
+def layout(request):
+    lay = request.param
+    nexus.scorer_layout(lay)
+    yield lay
+    nexus.scorer_layout(0)
+
+
+def _layout_case(name, lay):
+    wl = CASES[name]
+    if lay == 2 and (wl.window > 32 or wl.dtype != "bf16"):
+        pytest.skip("two pipelines per CTA cover bf16 windows of up to 32 rows")
+    return wl
+
+
+def _check_layout_used(lay):
+    if lay == 2:
+        assert nexus.scorer_config()["teams_per_cta"] == 2, nexus.scorer_config()
+
 
 def _decode(c, q, wl):
     k = c["k"][0, 0, 0, : int(c["lens"].reshape(-1)[0])]
@@ -45,9 +69,10 @@ def _decode(c, q, wl):
     return k.astype(np.float64), qbar
 
 
+@pytest.mark.parametrize("layout", LAYOUTS, indirect=True)
 @pytest.mark.parametrize("name", list(CASES))
-def test_scores_and_walk_match_oracle(name):
-    wl = CASES[name]
+def test_scores_and_walk_match_oracle(name, layout):
+    wl = _layout_case(name, layout)
     run = GpuRun(wl)
     S, cap, Wn = run.cache.n_slices, wl.capacity, wl.window
     a = torch.full((S, cap), -1.0, device=DEV)
@@ -57,6 +82,7 @@ def test_scores_and_walk_match_oracle(name):
     nexus.direct_scores(run.cache, run.q, run.params, a, stats, run.ws, run.status)
     nexus.walk(run.cache, run.q, run.params, w, ct, run.ws, run.status)
     run.check_status()
+    _check_layout_used(layout)
     a, stats, w, ct = a.cpu().numpy(), stats.cpu().numpy(), w.cpu().numpy(), ct.cpu().numpy()
     lens = run.lens()
     for sid in range(S):
@@ -123,14 +149,16 @@ def test_compact_bitexact_on_oracle_keep(name):
             assert torch.equal(run.d["k"][layer, s, h, nl:], k_before[layer, s, h, nl:])
 
 
+@pytest.mark.parametrize("layout", LAYOUTS, indirect=True)
 @pytest.mark.parametrize("name", list(CASES))
-def test_evict_step_end_to_end(name):
-    wl = CASES[name]
+def test_evict_step_end_to_end(name, layout):
+    wl = _layout_case(name, layout)
     run = GpuRun(wl)
     S = run.cache.n_slices
     lens0 = run.lens()
     nexus.evict_step(run.cache, run.q, run.params, run.keep, run.ws, run.status)
     run.check_status()
+    _check_layout_used(layout)
     keep = run.keep.cpu().numpy()
     lens = run.lens()
     for sid in range(S):
