@@ -501,6 +501,8 @@ struct Epi {
   // tiles whose TMEM loads share one wait, per pass (two measured slower than one: the
   // passes are bound by arithmetic and barriers, not by the load latency)
   static constexpr int P1a = 1, P1b = 1, P2 = 1;
+  // per-column coefficients kept in registers across the tiles (when few enough)
+  static constexpr bool kHoist = CW <= 8;
   const Args& A;
   uint8_t* sm;
   uint32_t tmem;
@@ -538,6 +540,9 @@ struct Epi {
   __device__ bool row_valid(const Chunk& ch, int t) {
     return ch.j0 + t * kTileRows + lg * 32 + lane < ch.T;
   }
+  __device__ bool tile_full(const Chunk& ch, int t) {
+    return ch.j0 + (t + 1) * kTileRows <= ch.T;
+  }
 
   // Passes 1a/1b: chunk maxima, e = exp((l - max)/sqrt(d)) written back to TMEM, chunk
   // sums and the walk-row Gram; the record goes to global memory.
@@ -556,10 +561,16 @@ struct Epi {
       tmem_ld_wait();
 #pragma unroll
       for (int u = 0; u < P1a; ++u) {
-        const bool valid = t0 + u < ch.ntiles && row_valid(ch, t0 + u);
+        if (t0 + u >= ch.ntiles) break;
+        if (kHoist && tile_full(ch, t0 + u)) {   // warp-uniform: no per-row test
 #pragma unroll
-        for (int i = 0; i < CW; ++i)
-          mx[i] = fmaxf(mx[i], valid ? __uint_as_float(r[u][i]) : -INFINITY);
+          for (int i = 0; i < CW; ++i) mx[i] = fmaxf(mx[i], __uint_as_float(r[u][i]));
+        } else {
+          const bool valid = row_valid(ch, t0 + u);
+#pragma unroll
+          for (int i = 0; i < CW; ++i)
+            mx[i] = fmaxf(mx[i], valid ? __uint_as_float(r[u][i]) : -INFINITY);
+        }
       }
     }
     if (tid == 0) trace_ev(A, vcta, nev, 10);
@@ -578,10 +589,11 @@ struct Epi {
     }
     epi_sync<NWG>(bar_id);
     if (tid == 0) trace_ev(A, vcta, nev, 11);
-    float z[CW], gp[kMaxPairs];
+    float z[CW], gp[kMaxPairs], snm[kHoist ? CW : 1];
 #pragma unroll
     for (int i = 0; i < CW; ++i) {
       z[i] = 0.f;
+      if (kHoist) snm[i] = nm()[col0 + i];
     }
 #pragma unroll
     for (int i = 0; i < kMaxPairs; ++i) gp[i] = 0.f;
@@ -596,12 +608,12 @@ struct Epi {
       for (int u = 0; u < P1b; ++u) {
         const int t = t0 + u;
         if (t >= ch.ntiles) break;
-        const bool valid = row_valid(ch, t);
+        const bool valid = (kHoist && tile_full(ch, t)) || row_valid(ch, t);
         float v[CW];
 #pragma unroll
         for (int i = 0; i < CW; ++i) {
-          const float e =
-              valid ? ex2_approx(fmaf(__uint_as_float(r[u][i]), cl2, nm()[col0 + i])) : 0.f;
+          const float sh = kHoist ? snm[i] : nm()[col0 + i];
+          const float e = valid ? ex2_approx(fmaf(__uint_as_float(r[u][i]), cl2, sh)) : 0.f;
           v[i] = e;
           z[i] += e;
         }
@@ -719,9 +731,11 @@ struct Epi {
     if (tid == 0) trace_ev(A, vcta, nev, 6);
     // partial sums over this warpgroup's columns for every tile, one barrier, then each
     // warpgroup finalizes a quarter of the tiles
-    float scc[kMaxWalk];
+    float scc[kMaxWalk], sca[kHoist ? CW : 1];
 #pragma unroll
     for (int tt = 0; tt < kMaxWalk; ++tt) scc[tt] = cc()[tt];
+#pragma unroll
+    for (int i = 0; i < (kHoist ? CW : 0); ++i) sca[i] = ca()[col0 + i];
     const int row = lg * 32 + lane;
     for (int t0 = 0; t0 < ch.ntiles; t0 += P2) {
       uint32_t r[P2][CW];
@@ -738,7 +752,8 @@ struct Epi {
         for (int i = 0; i < CW; ++i) v[i] = __uint_as_float(r[u][i]);
         float a4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < CW; ++i) a4[i & 3] = fmaf(v[i], ca()[col0 + i], a4[i & 3]);
+        for (int i = 0; i < CW; ++i)
+          a4[i & 3] = fmaf(v[i], kHoist ? sca[i] : ca()[col0 + i], a4[i & 3]);
         apart()[(t * NWG + wg) * kTileRows + row] = (a4[0] + a4[1]) + (a4[2] + a4[3]);
         if (wg == kWalkWg) {
           float ct = 0.f;
