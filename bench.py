@@ -59,6 +59,38 @@ def parse_args():
     return ap.parse_args()
 
 
+# source file of each kernel, for matching the DRAM traffic recorded under profiles/
+KERNEL_SOURCES = {"score_tc": "nx_score_tc.cu", "select": "nx_select.cu",
+                  "compact": "nx_compact.cu", "prep": "nx_score.cu"}
+
+
+def _source_digest(kernel: str) -> str | None:
+    import hashlib
+    name = KERNEL_SOURCES.get(kernel)
+    if name is None:
+        return None
+    path = os.path.join(ROOT, "streaming_kv_cache_step_gb300", "csrc", name)
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str) -> int | None:
+    """DRAM bytes (read + write) of one launch, from the counter capture recorded in
+    profiles/traffic.txt, when it was taken of this kernel source on this workload; None
+    once the kernel has changed since (or when there is no capture)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    digest = _source_digest(kernel)
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) == 4 and not line.startswith("#") and parts[0] == kernel \
+                    and parts[1] == workload and parts[2] == digest:
+                return int(parts[3])
+    return None
+
+
 def measured_peaks() -> dict:
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -327,7 +359,8 @@ def run_native(args, rank, world, local):
     step_gbs = ab["total"] / (statistics.mean(step_ms) * 1e-3) / 1e9
     roofline = dict(bound="hbm", kernel=dom_name, achieved=round(achieved, 1),
                     peak=peaks["hbm_gbs"], unit="GB/s",
-                    frac=round(achieved / peaks["hbm_gbs"], 4), traffic=None,
+                    frac=round(achieved / peaks["hbm_gbs"], 4),
+                    traffic=recorded_traffic(dom_name, wl.name), alg_bytes=int(dom_bytes),
                     peak_source=peaks["src"],
                     whole_step=dict(achieved=round(step_gbs, 1),
                                     frac=round(step_gbs / peaks["hbm_gbs"], 4),
@@ -382,6 +415,8 @@ def run_native(args, rank, world, local):
                roofline=roofline,
                e2e=dict(value=round(e2e_value, 1), unit=UNIT, h2d_bytes_per_step=h2d,
                         d2h_bytes_per_step=d2h, steps=e2e_steps),
+               ms_per_step_median=round(statistics.median(step_ms), 5),
+               per_sequence_tokens_per_s=round(value / (wl.layers * wl.kv_heads), 1),
                gpu_launches=launches, kernels_us={k: round(v, 3) for k, v in per_kernel.items()},
                scorer=scorer_cfg, eager=eager,
                clocks=clocks)

@@ -92,9 +92,12 @@ compact_kernel(nx_cache c, const int32_t* __restrict__ keep, const int32_t* __re
   uint4* bufs = reinterpret_cast<uint4*>(smem);
   __shared__ int s_src[2][kCompactRows];
   __shared__ int s_pos[2][kCompactRows];
+  __shared__ long long s_srow[2][kCompactRows];   // source and destination row indices
+  __shared__ long long s_drow[2][kCompactRows];
   __shared__ TileSlot s_slot[2];
   __shared__ long long s_claim;
   __shared__ int s_ok;
+  grid_dep_wait();                 // kept slots and new lengths come from the kernels before
   uint4* K = reinterpret_cast<uint4*>(c.k);
   uint4* V = reinterpret_cast<uint4*>(c.v);
 
@@ -120,7 +123,12 @@ compact_kernel(nx_cache c, const int32_t* __restrict__ keep, const int32_t* __re
       const int src = (i < sl.n) ? kp[sl.i0 + i] : 0;
       s_src[b][i] = src;
       const bool mv = i < sl.n && src != sl.i0 + i;
-      if (mv) s_pos[b][i] = c.pos[row_of(c, sl.l, sl.s, sl.h, src)];
+      if (mv) {
+        const long long sr = row_of(c, sl.l, sl.s, sl.h, src);
+        s_srow[b][i] = sr;
+        s_drow[b][i] = row_of(c, sl.l, sl.s, sl.h, sl.i0 + i);
+        s_pos[b][i] = c.pos[sr];
+      }
       const unsigned any = __ballot_sync(0xffffffffu, mv);
       if (i == 0) {
         sl.moves = any != 0;
@@ -134,9 +142,8 @@ compact_kernel(nx_cache c, const int32_t* __restrict__ keep, const int32_t* __re
       uint4* bv = bk + kCompactRows * chunks;
       for (int e = threadIdx.x; e < sl.n * chunks; e += blockDim.x) {
         const int i = e / chunks, ch = e - i * chunks;
-        const int src = s_src[b][i];
-        if (src != sl.i0 + i) {
-          const long long r = row_of(c, sl.l, sl.s, sl.h, src);
+        if (s_src[b][i] != sl.i0 + i) {
+          const long long r = s_srow[b][i];
           cp_async16(bk + e, K + r * chunks + ch);
           cp_async16(bv + e, V + r * chunks + ch);
         }
@@ -154,8 +161,9 @@ compact_kernel(nx_cache c, const int32_t* __restrict__ keep, const int32_t* __re
     cp_async_wait_all();
     __syncthreads();
     if (threadIdx.x == 0) {
-      __threadfence();
-      if (cur.tile != skip_signal_tile) st_release(tile_flags + cur.tile, 1);   // test hook
+      // the release store orders the block's completed reads (barrier above) before the
+      // flag; tiles past the slice's new length are read by no later tile of the slice
+      if (cur.n > 0 && cur.tile != skip_signal_tile) st_release(tile_flags + cur.tile, 1);
       if (cur.t == 0 && cur.tile < total_tiles && cur.nl >= 0) c.lens[cur.slice] = cur.nl;
       s_ok = 1;
     }
@@ -174,13 +182,13 @@ compact_kernel(nx_cache c, const int32_t* __restrict__ keep, const int32_t* __re
         for (int e = threadIdx.x; e < cur.n * chunks; e += blockDim.x) {
           const int i = e / chunks, ch = e - i * chunks;
           if (s_src[b][i] != cur.i0 + i) {
-            const long long r = row_of(c, cur.l, cur.s, cur.h, cur.i0 + i);
+            const long long r = s_drow[b][i];
             K[r * chunks + ch] = bk[e];
             V[r * chunks + ch] = bv[e];
           }
         }
         if (threadIdx.x < cur.n && s_src[b][threadIdx.x] != cur.i0 + (int)threadIdx.x)
-          c.pos[row_of(c, cur.l, cur.s, cur.h, cur.i0 + threadIdx.x)] = s_pos[b][threadIdx.x];
+          c.pos[s_drow[b][threadIdx.x]] = s_pos[b][threadIdx.x];
       }
     }
     __syncthreads();
@@ -213,9 +221,11 @@ cudaError_t launch_compact(const nx_cache& c, const nx_params& p, const WsLayout
   long long grid = (long long)sms * (per_sm > 0 ? per_sm : 1);
   if (grid > total) grid = total;
   if (grid < 1) grid = 1;
-  compact_kernel<<<(unsigned)grid, kCompactThreads, smem, st>>>(
-      c, keep, newlen, reinterpret_cast<int*>(ws + L.tile_flags),
-      reinterpret_cast<unsigned long long*>(ws + L.work), L.tiles_per_slice, total, dev_status, skip_signal_tile);
+  const cudaError_t e = launch_after(
+      compact_kernel, dim3((unsigned)grid), dim3(kCompactThreads), smem, st, c, keep, newlen,
+      reinterpret_cast<int*>(ws + L.tile_flags), reinterpret_cast<unsigned long long*>(ws + L.work),
+      (int)L.tiles_per_slice, total, dev_status, skip_signal_tile);
+  if (e != cudaSuccess) return e;
   note_launch(st, launches, "compact");
   return cudaGetLastError();
 }

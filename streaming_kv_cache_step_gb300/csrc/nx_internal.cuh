@@ -4,6 +4,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <utility>
 #include <stdint.h>
 
 #include "nexus.h"
@@ -195,6 +196,34 @@ struct ScoreOut {
   uint32_t* keys;    // [slices][cap]
   int flags;
 };
+
+// Programmatic dependent launch. A kernel launched with launch_after() may be scheduled
+// while the kernel before it on the stream is still running: it calls grid_dep_wait()
+// before touching anything that kernel writes (the wait returns once that kernel has
+// completed and its memory operations are visible; it returns at once when there is no
+// such dependency). grid_dep_trigger() lets the next kernel be scheduled early.
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_after(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                         cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // nx_score.cu
 cudaError_t launch_prep(const nx_cache& c, const void* q, const nx_params& p, const WsLayout& L,

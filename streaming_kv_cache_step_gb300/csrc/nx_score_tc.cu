@@ -1069,6 +1069,9 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the setup above overlaps the previous kernel; its outputs are read only from here on
+  grid_dep_trigger();
+  grid_dep_wait();
   const uint32_t tmem = *tmem_slot + (uint32_t)team * team_cols;   // column offset
   volatile int* abort_flag = ctl + 1;
   if (tid == 0) trace_mark(A, vcta, 1, 9);
@@ -1343,12 +1346,19 @@ cudaError_t launch_t(const nx_cache& c, const nx_params& p, const void* q, const
     cfg.blockDim = dim3(R::kBlockThreads);
     cfg.dynamicSmemBytes = S::kAlloc;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     cudaError_t e = cudaLaunchKernelEx(&cfg, score_tc_kernel<W, D, NWG>, map, a);
+    if (e == cudaErrorInvalidValue || e == cudaErrorNotSupported) {
+      (void)cudaGetLastError();            // without the early start, then
+      cfg.numAttrs = 1;
+      e = cudaLaunchKernelEx(&cfg, score_tc_kernel<W, D, NWG>, map, a);
+    }
     if (e == cudaErrorCooperativeLaunchTooLarge) {
       (void)cudaGetLastError();
       g_last_cfg[0] = -5;

@@ -95,6 +95,8 @@ __global__ void __launch_bounds__(kSelThreads)
 select_kernel(nx_cache c, const uint32_t* __restrict__ keys, int32_t* __restrict__ keep,
               const int32_t* __restrict__ newlen) {
   extern __shared__ uint32_t s_keys[];
+  grid_dep_trigger();
+  grid_dep_wait();                 // keys and new lengths come from the kernels before
   const int slice = blockIdx.x;
   const int nl = newlen[slice];
   if (nl < 0) return;
@@ -214,9 +216,13 @@ cudaError_t launch_select(const nx_cache& c, const uint32_t* keys, int32_t* keep
       if (e != cudaSuccess) return e;
       attr_set[dev] = true;
     }
-    select_kernel<true><<<(unsigned)slices, kSelThreads, bytes, st>>>(c, keys, keep, newlen);
+    const cudaError_t e = launch_after(select_kernel<true>, dim3((unsigned)slices),
+                                       dim3(kSelThreads), bytes, st, c, keys, keep, newlen);
+    if (e != cudaSuccess) return e;
   } else {
-    select_kernel<false><<<(unsigned)slices, kSelThreads, 0, st>>>(c, keys, keep, newlen);
+    const cudaError_t e = launch_after(select_kernel<false>, dim3((unsigned)slices),
+                                       dim3(kSelThreads), 0, st, c, keys, keep, newlen);
+    if (e != cudaSuccess) return e;
   }
   note_launch(st, launches, "select");
   return cudaGetLastError();
