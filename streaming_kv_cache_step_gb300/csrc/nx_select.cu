@@ -6,7 +6,7 @@
 // largest kappa, ties to the newer slot. One thread block per slice finds the B-th
 // largest composite by an MSB-first radix select (four 8-bit digit passes on the key,
 // four more on the slot only when the threshold key is tied), then writes the kept
-// slots in ascending order with a block-wide ballot scan.
+// slots in ascending order (per-warp runs, ballots, one scan of the warp totals).
 #include "nx_internal.cuh"
 
 namespace nx {
@@ -67,26 +67,19 @@ __device__ __forceinline__ void pick_digit(const unsigned* hist, int need, int* 
   }
 }
 
-// Histogram of kDigitBits-bit digits of the elements matching a prefix, with
-// warp-aggregated shared-memory atomics (one atomic per distinct digit per warp).
+// Histogram of kDigitBits-bit digits of the elements matching a prefix, with plain
+// shared-memory atomics (measured faster than aggregating equal digits per warp first).
 template <bool SMEM>
 __device__ __forceinline__ void digit_hist(const uint32_t* keys, int T, uint32_t pmask,
                                            uint32_t prefix, int shift, bool by_slot,
                                            uint32_t tau, unsigned* hist) {
-  const int lane = threadIdx.x & 31;
-  for (int j0 = 0; j0 < T; j0 += blockDim.x) {
-    const int j = j0 + threadIdx.x;
-    uint32_t digit = kBins;
-    if (j < T) {
-      const uint32_t k = keys[j];
-      if (!by_slot) {
-        if ((k & pmask) == prefix) digit = (k >> shift) & (kBins - 1u);
-      } else if (k == tau && ((uint32_t)j & pmask) == prefix) {
-        digit = ((uint32_t)j >> shift) & (kBins - 1u);
-      }
+  for (int j = threadIdx.x; j < T; j += blockDim.x) {
+    const uint32_t k = keys[j];
+    if (!by_slot) {
+      if ((k & pmask) == prefix) atomicAdd(&hist[(k >> shift) & (kBins - 1u)], 1u);
+    } else if (k == tau && ((uint32_t)j & pmask) == prefix) {
+      atomicAdd(&hist[((uint32_t)j >> shift) & (kBins - 1u)], 1u);
     }
-    const unsigned peers = __match_any_sync(0xffffffffu, digit);
-    if (digit < kBins && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], __popc(peers));
   }
 }
 
@@ -159,31 +152,38 @@ select_kernel(nx_cache c, const uint32_t* __restrict__ keys, int32_t* __restrict
     }
     slot_tau = (int)sp;
   }
-  // ---- write kept slots, ascending: ballot per warp, shuffle scan of the warp counts ----
+  // ---- write kept slots, ascending: every warp owns a contiguous run of slots, which it
+  // reads 32 at a time (ballots count and place its survivors); one scan of the warp
+  // totals gives each warp its output offset ----
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  int base = 0;
-  for (int j0 = 0; j0 < T; j0 += blockDim.x) {
-    const int j = j0 + threadIdx.x;
-    bool take = false;
-    if (j < T) {
-      const uint32_t k = kk[j];
-      take = (k > tau) || (k == tau && j >= slot_tau);
-    }
-    const unsigned bal = __ballot_sync(0xffffffffu, take);
-    if (lane == 0) wcount[warp] = __popc(bal);
-    __syncthreads();
-    int cw = lane < nw ? wcount[lane] : 0;          // every warp scans the warp counts
-    int incl = cw;
+  const int span = ((T + nw - 1) / nw + 31) / 32 * 32;
+  const int w0 = min(T, warp * span), w1 = min(T, w0 + span);
+  auto take = [&](int j) {
+    if (j >= w1) return false;
+    const uint32_t k = kk[j];
+    return (k > tau) || (k == tau && j >= slot_tau);
+  };
+  int cnt = 0;
+  for (int j0 = w0; j0 < w1; j0 += 32) cnt += __popc(__ballot_sync(0xffffffffu, take(j0 + lane)));
+  if (lane == 0) wcount[warp] = cnt;
+  __syncthreads();
+  if (warp == 0) {
+    const int cw = lane < nw ? wcount[lane] : 0;
+    int wi = cw;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
+      const int y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
     }
-    const int excl_w = __shfl_sync(0xffffffffu, incl - cw, warp);
-    const int tot = __shfl_sync(0xffffffffu, incl, 31);
-    if (take) out[base + excl_w + __popc(bal & ((1u << lane) - 1u))] = j;
-    base += tot;
-    __syncthreads();
+    if (lane < nw) wcount[lane] = wi - cw;        // exclusive prefix of the warp totals
+  }
+  __syncthreads();
+  int o = wcount[warp];
+  for (int j0 = w0; j0 < w1; j0 += 32) {
+    const bool t = take(j0 + lane);
+    const unsigned bal = __ballot_sync(0xffffffffu, t);
+    if (t) out[o + __popc(bal & ((1u << lane) - 1u))] = j0 + lane;
+    o += __popc(bal);
   }
 }
 
