@@ -73,12 +73,25 @@ template <bool SMEM>
 __device__ __forceinline__ void digit_hist(const uint32_t* keys, int T, uint32_t pmask,
                                            uint32_t prefix, int shift, bool by_slot,
                                            uint32_t tau, unsigned* hist) {
-  for (int j = threadIdx.x; j < T; j += blockDim.x) {
-    const uint32_t k = keys[j];
-    if (!by_slot) {
-      if ((k & pmask) == prefix) atomicAdd(&hist[(k >> shift) & (kBins - 1u)], 1u);
-    } else if (k == tau && ((uint32_t)j & pmask) == prefix) {
-      atomicAdd(&hist[((uint32_t)j >> shift) & (kBins - 1u)], 1u);
+  // (keys in global memory: U loads in flight per thread before their atomics)
+  constexpr int U = SMEM ? 1 : 8;
+  for (int j0 = threadIdx.x; j0 < T; j0 += U * blockDim.x) {
+    uint32_t kv[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int j = j0 + u * blockDim.x;
+      kv[u] = j < T ? keys[j] : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int j = j0 + u * blockDim.x;
+      if (j >= T) break;
+      const uint32_t k = kv[u];
+      if (!by_slot) {
+        if ((k & pmask) == prefix) atomicAdd(&hist[(k >> shift) & (kBins - 1u)], 1u);
+      } else if (k == tau && ((uint32_t)j & pmask) == prefix) {
+        atomicAdd(&hist[((uint32_t)j >> shift) & (kBins - 1u)], 1u);
+      }
     }
   }
 }
@@ -87,7 +100,7 @@ template <bool SMEM>
 __global__ void __launch_bounds__(kSelThreads)
 select_kernel(nx_cache c, const uint32_t* __restrict__ keys, int32_t* __restrict__ keep,
               const int32_t* __restrict__ newlen) {
-  extern __shared__ uint32_t s_keys[];
+  extern __shared__ __align__(16) uint32_t s_keys[];
   grid_dep_trigger();
   grid_dep_wait();                 // keys and new lengths come from the kernels before
   const int slice = blockIdx.x;
@@ -103,7 +116,29 @@ select_kernel(nx_cache c, const uint32_t* __restrict__ keys, int32_t* __restrict
   const uint32_t* gk = keys + (long long)slice * c.capacity;
   const uint32_t* kk = gk;
   if (SMEM) {
-    for (int j = threadIdx.x; j < T; j += blockDim.x) s_keys[j] = __ldcs(gk + j);
+    // stage the slice's keys: 16-byte loads, eight in flight per thread
+    int j_tail = 0;
+    if ((c.capacity & 3) == 0) {
+      const int nv = T >> 2;
+      const uint4* gv = reinterpret_cast<const uint4*>(gk);
+      uint4* sv = reinterpret_cast<uint4*>(s_keys);
+      constexpr int U = 8;
+      for (int v0 = threadIdx.x; v0 < nv; v0 += U * blockDim.x) {
+        uint4 x[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int v = v0 + u * blockDim.x;
+          if (v < nv) x[u] = __ldcs(gv + v);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int v = v0 + u * blockDim.x;
+          if (v < nv) sv[v] = x[u];
+        }
+      }
+      j_tail = nv * 4;
+    }
+    for (int j = j_tail + threadIdx.x; j < T; j += blockDim.x) s_keys[j] = __ldcs(gk + j);
     kk = s_keys;
     __syncthreads();
   }
@@ -158,13 +193,28 @@ select_kernel(nx_cache c, const uint32_t* __restrict__ keys, int32_t* __restrict
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const int span = ((T + nw - 1) / nw + 31) / 32 * 32;
   const int w0 = min(T, warp * span), w1 = min(T, w0 + span);
-  auto take = [&](int j) {
-    if (j >= w1) return false;
-    const uint32_t k = kk[j];
-    return (k > tau) || (k == tau && j >= slot_tau);
+  // (keys in global memory: U rows of 32 loads in flight per warp)
+  constexpr int U = SMEM ? 1 : 8;
+  auto load = [&](int j0, bool (&t)[U]) {
+    uint32_t kv[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int j = j0 + 32 * u + lane;
+      kv[u] = j < w1 ? kk[j] : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int j = j0 + 32 * u + lane;
+      t[u] = j < w1 && ((kv[u] > tau) || (kv[u] == tau && j >= slot_tau));
+    }
   };
   int cnt = 0;
-  for (int j0 = w0; j0 < w1; j0 += 32) cnt += __popc(__ballot_sync(0xffffffffu, take(j0 + lane)));
+  for (int j0 = w0; j0 < w1; j0 += 32 * U) {
+    bool t[U];
+    load(j0, t);
+#pragma unroll
+    for (int u = 0; u < U; ++u) cnt += __popc(__ballot_sync(0xffffffffu, t[u]));
+  }
   if (lane == 0) wcount[warp] = cnt;
   __syncthreads();
   if (warp == 0) {
@@ -179,11 +229,15 @@ select_kernel(nx_cache c, const uint32_t* __restrict__ keys, int32_t* __restrict
   }
   __syncthreads();
   int o = wcount[warp];
-  for (int j0 = w0; j0 < w1; j0 += 32) {
-    const bool t = take(j0 + lane);
-    const unsigned bal = __ballot_sync(0xffffffffu, t);
-    if (t) out[o + __popc(bal & ((1u << lane) - 1u))] = j0 + lane;
-    o += __popc(bal);
+  for (int j0 = w0; j0 < w1; j0 += 32 * U) {
+    bool t[U];
+    load(j0, t);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const unsigned bal = __ballot_sync(0xffffffffu, t[u]);
+      if (t[u]) out[o + __popc(bal & ((1u << lane) - 1u))] = j0 + 32 * u + lane;
+      o += __popc(bal);
+    }
   }
 }
 
