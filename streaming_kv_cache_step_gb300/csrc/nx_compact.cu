@@ -3,7 +3,8 @@
 //
 // keep is ascending with keep[i] >= i, so writing row i can only destroy a source that a
 // destination i' <= i still needs. Destinations are cut into tiles of kCompactRows rows,
-// claimed in increasing order through one global counter. A tile first copies all its
+// claimed in increasing order through one global counter (which skips the empty tail
+// tiles of each slice). A tile first copies all its
 // sources into shared memory, then publishes "read done", then waits (bounded) until the
 // earlier tiles of its slice have published, and only then writes. Each block holds two
 // tiles: the next one's reads (cp.async) overlap the current one's wait and writes.
@@ -103,7 +104,21 @@ compact_kernel(nx_cache c, const int32_t* __restrict__ keep, const int32_t* __re
 
   // claim the next tile (in increasing order over the whole grid) and start its reads
   auto stage = [&](int b) {
-    if (threadIdx.x == 0) s_claim = (long long)atomicAdd(work, 1ULL);
+    if (threadIdx.x == 0) {
+      // Claim the next tile; tiles past their slice's new length (and every tile of a
+      // rejected slice) hold no rows and are waited on by nobody, so once one is met the
+      // counter jumps to the next slice. Tile 0 of a valid slice is always taken (it
+      // writes the new length).
+      long long x = (long long)atomicAdd(work, 1ULL);
+      while (x < total_tiles) {
+        const int sx = (int)(x / tiles_per_slice), tx = (int)(x % tiles_per_slice);
+        const int nx = newlen[sx];
+        if (nx >= 0 && (tx == 0 || tx * kCompactRows < nx)) break;
+        atomicMax(work, (unsigned long long)(sx + 1) * (unsigned long long)tiles_per_slice);
+        x = (long long)atomicAdd(work, 1ULL);
+      }
+      s_claim = x;
+    }
     __syncthreads();
     TileSlot sl;
     sl.tile = s_claim;
@@ -118,23 +133,21 @@ compact_kernel(nx_cache c, const int32_t* __restrict__ keep, const int32_t* __re
       if (sl.nl >= 0 && sl.i0 < sl.nl) sl.n = min(kCompactRows, sl.nl - sl.i0);
     }
     const int32_t* kp = (sl.n > 0) ? keep + (long long)sl.slice * c.capacity : nullptr;
+    bool mv = false;
     if (threadIdx.x < kCompactRows) {
       const int i = threadIdx.x;
       const int src = (i < sl.n) ? kp[sl.i0 + i] : 0;
       s_src[b][i] = src;
-      const bool mv = i < sl.n && src != sl.i0 + i;
+      mv = i < sl.n && src != sl.i0 + i;
       if (mv) {
         const long long sr = row_of(c, sl.l, sl.s, sl.h, src);
         s_srow[b][i] = sr;
         s_drow[b][i] = row_of(c, sl.l, sl.s, sl.h, sl.i0 + i);
         s_pos[b][i] = c.pos[sr];
       }
-      const unsigned any = __ballot_sync(0xffffffffu, mv);
-      if (i == 0) {
-        sl.moves = any != 0;
-        s_slot[b] = sl;
-      }
     }
+    sl.moves = __syncthreads_or(mv);      // any row of the tile moves
+    if (threadIdx.x == 0) s_slot[b] = sl;
     __syncthreads();
     sl = s_slot[b];
     if (sl.moves) {
@@ -215,6 +228,11 @@ cudaError_t launch_compact(const nx_cache& c, const nx_params& p, const WsLayout
   const size_t smem = 2 * 2 * (size_t)kCompactRows * row_bytes;   // two buffers of K + V
   int dev = 0, sms = 0, per_sm = 0;
   cudaGetDevice(&dev);
+  if (smem > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        compact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, compact_kernel, kCompactThreads, smem);
   const long long total = L.slices * L.tiles_per_slice;

@@ -2,22 +2,25 @@
 // (bf16 caches, head_dim 64 or 128, W in {16, 32, 64}, contiguous or paged).
 //
 // Nexus Sampling paper, §2.1 Eq. (1) (b = 1), §2.2 Eqs. (2)-(5), §2.3 (keys of Eq. (6),
-// n = 1). One persistent, cooperatively launched kernel; two CTAs per SM. A CTA takes
-// chunks of up to 256/W tiles of 128 cached rows of one slice and:
-//   1. stages each K tile in shared memory with TMA (128-byte swizzle, one box per
-//      64-element column block -- per page when paged), double-buffered;
-//   2. one thread issues tcgen05.mma (kind::f16, bf16 x bf16 -> fp32), M = 128 rows,
+// n = 1). One persistent, cooperatively launched kernel, one CTA per SM, holding one or
+// two pipelines ("teams"). A pipeline takes chunks of up to 8 tiles of 128 cached rows of
+// one slice (the chunk schedule below) and:
+//   1. a TMA producer thread stages each K tile in a ring of shared-memory stages
+//      (128-byte swizzle, one box per 64-element column block -- per page when paged);
+//   2. an MMA thread issues tcgen05.mma (kind::f16, bf16 x bf16 -> fp32), M = 128 rows,
 //      N = W window rows, K = head_dim, twice: against bf16(Qbar) and against
-//      bf16(Qbar - bf16(Qbar)), accumulating in the same TMEM columns, so the logits
-//      keep fp32 accuracy although the tensor cores take bf16 operands. Every tile's
-//      logits stay in TMEM (tile t -> columns [t*W, (t+1)*W)) until the chunk is done;
-//   3. four epilogue warps (one TMEM lane = one row each) take the chunk maxima, then
-//      e = exp((l - max_chunk)/sqrt(d)) written back to TMEM, the chunk sums and the
-//      H x H Gram of the walk rows, and publish them;
-//   4. a bounded slice-wide barrier: the last chunk of the slice to arrive merges all
-//      chunk statistics, runs the walk recurrence (gamma_t = 1 + sum_{u<t} gamma_u
-//      <P_t, P_u>, the rank-1 form of Eq. (4)) and publishes the per-row coefficients;
-//   5. every chunk turns its TMEM e values into a, c~, w and the order key of every row.
+//      bf16(Qbar - bf16(Qbar)), accumulating in the same TMEM columns, so the logits keep
+//      fp32 accuracy although the tensor cores take bf16 operands. A chunk's logits fill
+//      one of two or three TMEM buffers (tile t -> columns [t*W, (t+1)*W));
+//   3. the epilogue warpgroups (one TMEM lane = one row) take the chunk maxima, write
+//      e = exp((l - max_chunk)/sqrt(d)) back to TMEM, and store the chunk record (maxima,
+//      sums, the H x H Gram of the walk rows); a publisher warp makes it visible and
+//      counts it into the slice;
+//   4. a merge warp waits (bounded) until every chunk of the slice is counted in, merges
+//      the slice's records, runs the walk recurrence (gamma_t = 1 + sum_{u<t} gamma_u
+//      <P_t, P_u>, the rank-1 form of Eq. (4)) and hands the per-row coefficients over;
+//   5. the epilogue turns the chunk's TMEM e values into a, c~, w and the order key of
+//      every row (one chunk behind step 3, so the slice wait overlaps the next chunk).
 // K is read from HBM exactly once; nothing but one key (and optional outputs) per row
 // goes back to memory.
 #include <cuda.h>
@@ -58,7 +61,7 @@ struct Args {
   nx_cache c;
   nx_params p;
   const unsigned char* qimg;   // [slices] shared-memory images of bf16 hi/lo queries
-  uint32_t tmem_cols;      // 256 with two CTAs per SM, 512 with one
+  uint32_t tmem_cols;      // columns the CTA allocates (all 512; split between its teams)
   int nbuf;                // TMEM buffers (2: the next chunk's MMAs overlap this epilogue)
   long long* trace;        // optional phase trace: [grid][kTraceEvents][2] (null: off)
   float* partial;          // [slices][maxc][stride]
@@ -1000,9 +1003,9 @@ __device__ void publish_warp(const Args& A, int chunk_rows, int nbuf, uint64_t* 
 }
 
 // A CTA's warps are dealt round-robin to the SM's four sub-partitions, each with 16K
-// registers: with NWG = 4 (20 warps, one CTA per SM) a sub-partition holds 5 warps, which
-// caps a thread at 96 registers; with NWG = 2 (12 warps, two CTAs per SM) it holds 6,
-// which caps a thread at 80.
+// registers: with NWG = 4 (one team of 20 warps) a sub-partition holds 5 warps, which caps
+// a thread at 96 registers; with NWG = 2 (two teams of 12 warps) it holds 6, which caps a
+// thread at 80.
 template <int W, int D, int NWG>
 __global__ void __launch_bounds__(Roles<NWG>::kBlockThreads, 1)
 score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
