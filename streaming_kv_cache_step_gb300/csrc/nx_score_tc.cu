@@ -54,6 +54,11 @@ struct Roles {
   static constexpr int kGroup = 32;                // records per bulk copy of the merge
 };
 constexpr int kTileRows = 128;
+// Who folds a chunk's max shift into the per-column weights: the merge warp (off the
+// epilogue's path) for windows of up to 32 rows; the epilogue for W = 64, whose merge warp
+// is already the slower side (measured).
+template <int W>
+constexpr bool kFoldInMerge = W <= 32;
 constexpr long long kWaitLimit = 1LL << 22;   // mbarrier polls before giving up
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -354,9 +359,9 @@ struct Smem {
   static constexpr int kOffMisc = kOffBar + 256;          // tmem slot + control words
   static constexpr int kOffRed = kOffMisc + 64;           // [kEpiWarps][kRedStride]
   static constexpr int kOffMc = kOffRed + R::kEpiWarps * kRedStride * 4;   // [3][W] chunk maxima
-  static constexpr int kOffCa = kOffMc + 3 * W * 4;       // [W] a coefficients
-  static constexpr int kOffCc = kOffCa + W * 4;           // [kMaxWalk] walk coefficients
-  static constexpr int kOffNm = kOffCc + kMaxWalk * 4;    // [W] -max * cl2 of the chunk
+  static constexpr int kOffCa = kOffMc + 3 * W * 4;       // [3][W] a coefficients
+  static constexpr int kOffCc = kOffCa + 3 * W * 4;       // [3][kMaxWalk] walk coefficients
+  static constexpr int kOffNm = kOffCc + 3 * kMaxWalk * 4;   // [W] -max * cl2 of the chunk
   static constexpr int kMrec = 2 * W + kMaxWalk;          // merged: max, normaliser, walk
   static constexpr int kOffMrec = kOffNm + W * 4;         // [3][kMrec] one per TMEM buffer
   static constexpr int kOffMs = kOffMrec + 3 * kMrec * 4; // merge warp scratch [2][W]
@@ -531,8 +536,12 @@ struct Epi {
   __device__ float* mc(uint32_t b) {
     return reinterpret_cast<float*>(sm + Smem<W, D, NWG>::kOffMc) + b * W;
   }
-  __device__ float* ca() { return reinterpret_cast<float*>(sm + Smem<W, D, NWG>::kOffCa); }
-  __device__ float* cc() { return reinterpret_cast<float*>(sm + Smem<W, D, NWG>::kOffCc); }
+  __device__ float* ca(uint32_t b) {
+    return reinterpret_cast<float*>(sm + Smem<W, D, NWG>::kOffCa) + b * W;
+  }
+  __device__ float* cc(uint32_t b) {
+    return reinterpret_cast<float*>(sm + Smem<W, D, NWG>::kOffCc) + b * kMaxWalk;
+  }
   __device__ float* nm() { return reinterpret_cast<float*>(sm + Smem<W, D, NWG>::kOffNm); }
   __device__ float* recs() { return reinterpret_cast<float*>(sm + Smem<W, D, NWG>::kOffRec); }
   __device__ float* apart() { return reinterpret_cast<float*>(sm + Smem<W, D, NWG>::kOffPart); }
@@ -716,29 +725,30 @@ struct Epi {
     epi_sync<NWG>(bar_id);
     if (tid == 0) trace_ev(A, vcta, nev, 5 + 1000 * (ch.slice + 1));
     if (ctl[2]) return false;
-    const float* mr = reinterpret_cast<const float*>(sm + S::kOffMrec) + ch.b * S::kMrec;
-    const float* m = mc(ch.b);
-    if (tid < W) {
-      const int w = tid;
-      // fold this chunk's max shift into the slice's per-row weights
-      const float shift = exp2f((m[w] - mr[w]) * cl2);
-      ca()[w] = shift / ((float)W * mr[W + w]);
-      if (w >= W - H) cc()[w - (W - H)] = mr[2 * W + (w - (W - H))] * shift;
+    if (!kFoldInMerge<W>) {
+      const float* mr = reinterpret_cast<const float*>(sm + S::kOffMrec) + ch.b * S::kMrec;
+      const float* m = mc(ch.b);
+      if (tid < W) {
+        const int w = tid;
+        // fold this chunk's max shift into the slice's per-column weights
+        const float shift = exp2f((m[w] - mr[w]) * cl2);
+        ca(ch.b)[w] = shift / ((float)W * mr[W + w]);
+        if (w >= W - H) cc(ch.b)[w - (W - H)] = mr[2 * W + (w - (W - H))] * shift;
+        if (ch.k == 0 && (A.out.flags & kEmitStats)) {
+          A.out.row_stats[((long long)ch.slice * W + w) * 2] = mr[w] * rsqrtf((float)D);
+          A.out.row_stats[((long long)ch.slice * W + w) * 2 + 1] = mr[W + w];
+        }
+      }
+      epi_sync<NWG>(bar_id);
     }
-    if (ch.k == 0 && (A.out.flags & kEmitStats) && tid < W) {
-      const int w = tid;
-      A.out.row_stats[((long long)ch.slice * W + w) * 2] = mr[w] * rsqrtf((float)D);
-      A.out.row_stats[((long long)ch.slice * W + w) * 2 + 1] = mr[W + w];
-    }
-    epi_sync<NWG>(bar_id);
     if (tid == 0) trace_ev(A, vcta, nev, 6);
     // partial sums over this warpgroup's columns for every tile, one barrier, then each
     // warpgroup finalizes a quarter of the tiles
     float scc[kMaxWalk], sca[kHoist ? CW : 1];
 #pragma unroll
-    for (int tt = 0; tt < kMaxWalk; ++tt) scc[tt] = cc()[tt];
+    for (int tt = 0; tt < kMaxWalk; ++tt) scc[tt] = cc(ch.b)[tt];
 #pragma unroll
-    for (int i = 0; i < (kHoist ? CW : 0); ++i) sca[i] = ca()[col0 + i];
+    for (int i = 0; i < (kHoist ? CW : 0); ++i) sca[i] = ca(ch.b)[col0 + i];
     const int row = lg * 32 + lane;
     for (int t0 = 0; t0 < ch.ntiles; t0 += P2) {
       uint32_t r[P2][CW];
@@ -756,7 +766,7 @@ struct Epi {
         float a4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < CW; ++i)
-          a4[i & 3] = fmaf(v[i], kHoist ? sca[i] : ca()[col0 + i], a4[i & 3]);
+          a4[i & 3] = fmaf(v[i], kHoist ? sca[i] : ca(ch.b)[col0 + i], a4[i & 3]);
         apart()[(t * NWG + wg) * kTileRows + row] = (a4[0] + a4[1]) + (a4[2] + a4[3]);
         if (wg == kWalkWg) {
           float ct = 0.f;
@@ -832,13 +842,16 @@ struct Epi {
     sched_init(sc, vcta, vgrid);
     int sl, kq, Tq;
     for (; sched_next(A, sc, chunk_rows, sl, kq, Tq); ++cnt) {
-      if (tid == 0) ctl[3] = ctl[1];   // one snapshot of the abort flag for all
+      const Chunk ch = make_chunk(A, sl, kq, Tq, chunk_rows, cnt, nbuf);
+      // thread 0 takes one snapshot of the abort flag and waits for the chunk's logits;
+      // everyone acts on both after the barrier
+      if (tid == 0) {
+        trace_ev(A, vcta, nev, 100 + ch.k);
+        ctl[3] = ctl[1];
+        ctl[2] = (!ctl[3] && mbar_wait(&bar_tfull[ch.b], ch.use & 1, A.dev_status)) ? 1 : 0;
+      }
       epi_sync<NWG>(bar_id);
       if (ctl[3]) break;
-      const Chunk ch = make_chunk(A, sl, kq, Tq, chunk_rows, cnt, nbuf);
-      if (tid == 0) trace_ev(A, vcta, nev, 100 + ch.k);
-      if (tid == 0) ctl[2] = mbar_wait(&bar_tfull[ch.b], ch.use & 1, A.dev_status) ? 1 : 0;
-      epi_sync<NWG>(bar_id);
       const bool ok = ctl[2] != 0;
       tc_fence_after();
       if (tid == 0) trace_ev(A, vcta, nev, 1);
@@ -974,6 +987,27 @@ __device__ void merge_warp(const Args& A, uint8_t* sm, int chunk_rows, int nbuf,
       gsum += g;
     }
     if (lane < H) out[2 * W + lane] = gam / (gsum * ms[W + (W - H + lane)]);
+    __syncwarp();
+    // fold this chunk's max shift (its maxima are in shared memory, stored before the
+    // chunk was published) into the per-column weights the epilogue applies
+    if (kFoldInMerge<W>) {
+      const float* mch = reinterpret_cast<const float*>(sm + S::kOffMc) + ch.b * W;
+      float* ca = reinterpret_cast<float*>(sm + S::kOffCa) + ch.b * W;
+      float* cc = reinterpret_cast<float*>(sm + S::kOffCc) + ch.b * kMaxWalk;
+#pragma unroll
+      for (int q = 0; q < QW; ++q) {
+        const int c = lane + 32 * q;
+        if (c < W) {
+          const float shift = exp2f((mch[c] - M[q]) * cl2);
+          ca[c] = shift / ((float)W * Z[q]);
+          if (c >= W - H) cc[c - (W - H)] = out[2 * W + (c - (W - H))] * shift;
+          if (ch.k == 0 && (A.out.flags & kEmitStats)) {
+            A.out.row_stats[((long long)ch.slice * W + c) * 2] = M[q] * rsqrtf((float)D);
+            A.out.row_stats[((long long)ch.slice * W + c) * 2 + 1] = Z[q];
+          }
+        }
+      }
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(&bar_mfull[ch.b]);
   }
@@ -1255,6 +1289,7 @@ cudaError_t launch_t(const nx_cache& c, const nx_params& p, const void* q, const
     return cudaSuccess;
   }
 
+  if (L.stats_stride != S::kRecStride) { g_last_cfg[0] = -2; return cudaSuccess; }
   int dev = 0, sms = 0, per_sm_api = 0;
   cudaGetDevice(&dev);
   static bool attr_set[64] = {};
