@@ -361,9 +361,14 @@ struct Smem {
   static constexpr int kOffMc = kOffRed + R::kEpiWarps * kRedStride * 4;   // [3][W] chunk maxima
   static constexpr int kOffCa = kOffMc + 3 * W * 4;       // [3][W] a coefficients
   static constexpr int kOffCc = kOffCa + 3 * W * 4;       // [3][kMaxWalk] walk coefficients
-  static constexpr int kOffNm = kOffCc + 3 * kMaxWalk * 4;   // [W] -max * cl2 of the chunk
+  // [3][4][W] per TMEM buffer, lane quarter and column: the maximum over that quarter's
+  // rows of the chunk (the shift of its e values)
+  static constexpr int kOffMw = kOffCc + 3 * kMaxWalk * 4;
+  // [kEpiWarps][CW + kMaxWalk] each warp's pass-2 weights for its columns and walk rows
+  static constexpr int kWca = W / NWG + kMaxWalk;
+  static constexpr int kOffWca = kOffMw + 3 * 4 * W * 4;
   static constexpr int kMrec = 2 * W + kMaxWalk;          // merged: max, normaliser, walk
-  static constexpr int kOffMrec = kOffNm + W * 4;         // [3][kMrec] one per TMEM buffer
+  static constexpr int kOffMrec = kOffWca + R::kEpiWarps * kWca * 4;   // [3][kMrec]
   static constexpr int kOffMs = kOffMrec + 3 * kMrec * 4; // merge warp scratch [2][W]
   static constexpr int kOffPart = kOffMs + 2 * W * 4;
   // pass-2 partial a per tile, warpgroup and row; the walk term per tile and row
@@ -542,7 +547,12 @@ struct Epi {
   __device__ float* cc(uint32_t b) {
     return reinterpret_cast<float*>(sm + Smem<W, D, NWG>::kOffCc) + b * kMaxWalk;
   }
-  __device__ float* nm() { return reinterpret_cast<float*>(sm + Smem<W, D, NWG>::kOffNm); }
+  __device__ float* mw(uint32_t b) {   // [4][W] lane-quarter maxima of buffer b
+    return reinterpret_cast<float*>(sm + Smem<W, D, NWG>::kOffMw) + b * 4 * W;
+  }
+  __device__ float* wca() {            // this warp's pass-2 weights
+    return reinterpret_cast<float*>(sm + Smem<W, D, NWG>::kOffWca) + warp * Smem<W, D, NWG>::kWca;
+  }
   __device__ float* recs() { return reinterpret_cast<float*>(sm + Smem<W, D, NWG>::kOffRec); }
   __device__ float* apart() { return reinterpret_cast<float*>(sm + Smem<W, D, NWG>::kOffPart); }
   __device__ float* ctp() { return reinterpret_cast<float*>(sm + Smem<W, D, NWG>::kOffCt); }
@@ -586,27 +596,23 @@ struct Epi {
       }
     }
     if (tid == 0) trace_ev(A, vcta, nev, 10);
+    // Each warp shifts its own rows by its own column maxima (no barrier here); the
+    // record step below rescales the four lane quarters to the chunk maximum, and pass 2
+    // folds the same factor into its weights.
+    float* mwq = mw(ch.b) + lg * W;
 #pragma unroll
     for (int i = 0; i < CW; ++i) {
-      const float x = warp_max_redux(mx[i]);
-      if (lane == 0) red()[warp * RS + col0 + i] = x;
+      mx[i] = warp_max_redux(mx[i]);
+      if (lane == 0) mwq[col0 + i] = mx[i];
     }
-    epi_sync<NWG>(bar_id);
-    if (tid < W) {
-      const int col = tid, g = col / CW;
-      float x = red()[(4 * g) * RS + col];
-      for (int q = 1; q < 4; ++q) x = fmaxf(x, red()[(4 * g + q) * RS + col]);
-      m[col] = x;
-      nm()[col] = -x * cl2;
-    }
-    epi_sync<NWG>(bar_id);
     if (tid == 0) trace_ev(A, vcta, nev, 11);
     float z[CW], gp[kMaxPairs], snm[kHoist ? CW : 1];
 #pragma unroll
     for (int i = 0; i < CW; ++i) {
       z[i] = 0.f;
-      if (kHoist) snm[i] = nm()[col0 + i];
+      if (kHoist) snm[i] = -mx[i] * cl2;
     }
+    __syncwarp();
 #pragma unroll
     for (int i = 0; i < kMaxPairs; ++i) gp[i] = 0.f;
     const bool walk_wg = (wg == kWalkWg);
@@ -624,7 +630,7 @@ struct Epi {
         float v[CW];
 #pragma unroll
         for (int i = 0; i < CW; ++i) {
-          const float sh = kHoist ? snm[i] : nm()[col0 + i];
+          const float sh = kHoist ? snm[i] : -mwq[col0 + i] * cl2;
           const float e = valid ? ex2_approx(fmaf(__uint_as_float(r[u][i]), cl2, sh)) : 0.f;
           v[i] = e;
           z[i] += e;
@@ -673,16 +679,39 @@ struct Epi {
     }
     epi_sync<NWG>(bar_id);
     float* rec = A.partial + ((long long)ch.slice * A.maxc + ch.k) * A.stride;
+    const float* mwb = mw(ch.b);
     if (tid < W) {
       const int col = tid, g = col / CW;
-      float x = 0.f;
-      for (int q = 0; q < 4; ++q) x += red()[(4 * g + q) * RS + col];
-      rec[col] = m[col];                  // chunk max (raw)
+      float mq[4], mm = -INFINITY;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        mq[q] = mwb[q * W + col];
+        mm = fmaxf(mm, mq[q]);
+      }
+      float x = 0.f;                      // quarter sums rescaled to the chunk maximum
+#pragma unroll
+      for (int q = 0; q < 4; ++q) x += red()[(4 * g + q) * RS + col] * exp2f((mq[q] - mm) * cl2);
+      m[col] = mm;
+      rec[col] = mm;                      // chunk max (raw)
       rec[W + col] = x;                   // sum relative to it
     } else if (tid < W + kMaxPairs) {
       const int k = tid - W;
+      int u = 0, t = 0;
+      pair_of(k, u, t);
       float x = 0.f;
-      for (int q = 0; q < 4; ++q) x += red()[(4 * kWalkWg + q) * RS + W + k];
+      if (t < H) {
+        const int cp = W - H + u, cq = W - H + t;
+        float mp = -INFINITY, mq = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          mp = fmaxf(mp, mwb[q * W + cp]);
+          mq = fmaxf(mq, mwb[q * W + cq]);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          x += red()[(4 * kWalkWg + q) * RS + W + k] *
+               exp2f(((mwb[q * W + cp] - mp) + (mwb[q * W + cq] - mq)) * cl2);
+      }
       rec[2 * W + k] = x;                 // Gram entry
     }
   }
@@ -744,11 +773,31 @@ struct Epi {
     if (tid == 0) trace_ev(A, vcta, nev, 6);
     // partial sums over this warpgroup's columns for every tile, one barrier, then each
     // warpgroup finalizes a quarter of the tiles
+    // this warp's weights: the slice weights times the shift from its lane quarter's
+    // maxima (its e values' reference) to the chunk maxima
+    float* wc = wca();
+    {
+      const float* mwq = mw(ch.b) + lg * W;
+      const float* mcb = mc(ch.b);
+      if (lane < CW) {
+        const int col = col0 + lane;
+        wc[lane] = ca(ch.b)[col] * exp2f((mwq[col] - mcb[col]) * cl2);
+      } else if (lane < CW + kMaxWalk) {
+        const int tt = lane - CW;
+        float x = 0.f;
+        if (tt < H) {
+          const int col = W - H + tt;
+          x = cc(ch.b)[tt] * exp2f((mwq[col] - mcb[col]) * cl2);
+        }
+        wc[lane] = x;
+      }
+      __syncwarp();
+    }
     float scc[kMaxWalk], sca[kHoist ? CW : 1];
 #pragma unroll
-    for (int tt = 0; tt < kMaxWalk; ++tt) scc[tt] = cc(ch.b)[tt];
+    for (int tt = 0; tt < kMaxWalk; ++tt) scc[tt] = wc[CW + tt];
 #pragma unroll
-    for (int i = 0; i < (kHoist ? CW : 0); ++i) sca[i] = ca(ch.b)[col0 + i];
+    for (int i = 0; i < (kHoist ? CW : 0); ++i) sca[i] = wc[i];
     const int row = lg * 32 + lane;
     for (int t0 = 0; t0 < ch.ntiles; t0 += P2) {
       uint32_t r[P2][CW];
@@ -766,7 +815,7 @@ struct Epi {
         float a4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < CW; ++i)
-          a4[i & 3] = fmaf(v[i], kHoist ? sca[i] : ca(ch.b)[col0 + i], a4[i & 3]);
+          a4[i & 3] = fmaf(v[i], kHoist ? sca[i] : wc[i], a4[i & 3]);
         apart()[(t * NWG + wg) * kTileRows + row] = (a4[0] + a4[1]) + (a4[2] + a4[3]);
         if (wg == kWalkWg) {
           float ct = 0.f;
