@@ -307,3 +307,40 @@ def test_evict_step_replays_from_a_cuda_graph(name):
         assert torch.equal(run.keep, want_keep)
         for k in pristine:
             assert torch.equal(run.d[k], want[k]), k
+
+
+# degenerate lengths: an empty slice, one and two rows (the ramp's T - 1 = 0 case), exactly
+# the forced slots, one row past them, and a small eviction
+EDGE = W.shrink(W.llama3_8b_layer(), seqs=6, kv_heads=1,
+                lens=np.array([0, 1, 2, 64, 65, 200], np.int32), capacity=256,
+                budget=np.array([64, 64, 64, 64, 64, 100], np.int32), n_hubs=4)
+
+
+@pytest.mark.parametrize("layout", LAYOUTS, indirect=True)
+def test_degenerate_lengths_end_to_end(layout):
+    wl = EDGE
+    run = GpuRun(wl)
+    S, cap = run.cache.n_slices, wl.capacity
+    lens0 = run.lens()
+    w = torch.full((S, cap), -1.0, device=DEV)
+    ct = torch.full((S, cap), -1.0, device=DEV)
+    nexus.walk(run.cache, run.q, run.params, w, ct, run.ws, run.status)
+    run.check_status()
+    w = w.cpu().numpy()
+    nexus.evict_step(run.cache, run.q, run.params, run.keep, run.ws, run.status)
+    run.check_status()
+    _check_layout_used(layout)
+    keep = run.keep.cpu().numpy()
+    lens = run.lens()
+    for sid in range(S):
+        c, _, _, ref = oracle_slice(wl, sid)
+        T, nl = int(lens0[sid]), int(ref["newlen"][0])
+        assert lens[sid] == nl, (sid, lens[sid], nl)
+        assert np.all(np.abs(w[sid, :T] - ref["w"][0, :T]) <= score_tol(ref["w"][0, :T], T))
+        assert (w[sid, T:] == -1).all()
+        if nl:
+            kappa = oracle_kappa(wl, sid, ref["w"][0, :T], c["pos"][0, 0, 0, :T])
+            compare_survivors(keep[sid, :nl], ref["keep"][0, :nl], kappa)
+            for name_ in ("k", "v", "pos"):
+                got = W.storage_to_numpy(run.slice_rows(name_, sid, nl))
+                assert np.array_equal(got, c[name_][0, 0, 0][keep[sid, :nl]]), (sid, name_)
