@@ -1380,23 +1380,23 @@ cudaError_t launch_t(const nx_cache& c, const nx_params& p, const void* q, const
       for (int t = 1; t <= max_tiles; ++t) {
         const int mc = (int)((cap_tiles + t - 1) / t);
         if (mc > grid_max || mc > kMaxChunksPerSlice) continue;
-        long long cost, gsel;
-        if (R::kTeams == 1) {
+        // Estimated time: rounds of the grid x (the chunk's tiles + about four tiles' worth
+        // of fixed latency), 1.5x without a second buffer to overlap chunks. With two or
+        // more buffers the next chunk's statistics overlap a slice's wait, so every
+        // pipeline takes part and slices need not align with rounds (measured: 8-tile
+        // chunks over all SMs beat 7-tile chunks in aligned rounds); with one buffer a
+        // round holds whole slices (a slice split across rounds would stall its first
+        // chunks for a whole round).
+        long long rounds, gsel;
+        if (nb == 1) {
           const long long per = grid_max / mc;                 // whole slices per round
-          const long long rounds = (slices + per - 1) / per;
-          // deeper TMEM buffering overlaps more; ties go to fewer rounds
-          const int depth_cost = nb == 3 ? 20 : (nb == 2 ? 22 : 30);
-          cost = (rounds * t * depth_cost) * 4096 + rounds;
+          rounds = (slices + per - 1) / per;
           gsel = per * mc;
         } else {
-          // two pipelines per CTA overlap one another, so slices need not align with
-          // rounds: all pipelines take part, and a chunk costs its tiles plus about four
-          // tiles' worth of fixed latency; at least two TMEM buffers
-          if (nb < 2) continue;
-          const long long rounds = (slices * mc + grid_max - 1) / grid_max;
-          cost = (rounds * (t + 4)) * 4 + (3 - nb);
+          rounds = (slices * mc + grid_max - 1) / grid_max;
           gsel = grid_max;
         }
+        const long long cost = rounds * (t + 4) * (nb == 1 ? 3 : 2) * 4 + (3 - nb);
         if (best < 0 || cost < best) {
           best = cost;
           nbuf = nb;
