@@ -50,7 +50,7 @@ struct Roles {
   static constexpr int kTeams = NWG == 2 ? 2 : 1;
   static constexpr int kBlockThreads = kTeams * kThreads;
   static constexpr uint32_t kTmemCols = 512u / kTeams;      // one team's share
-  static constexpr int kMaxChunkTiles = 2 * NWG;   // the pass-2 partials are sized for it
+  static constexpr int kMaxChunkTiles = 8;         // the pass-2 partials are sized for it
   static constexpr int kGroup = 32;                // records per bulk copy of the merge
 };
 constexpr int kTileRows = 128;
@@ -734,10 +734,11 @@ struct Epi {
     int* ctl = reinterpret_cast<int*>(sm + S::kOffMisc + 16);
     const nx_cache& c = A.c;
     const nx_params& p = A.p;
-    // rows this thread finalizes: tiles t = wg, wg + NWG (at most two); positions first
-    int32_t posv[2];
+    // rows this thread finalizes: tiles t = wg, wg + NWG, ... (R2 of them); positions first
+    constexpr int R2 = Roles<NWG>::kMaxChunkTiles / NWG;
+    int32_t posv[R2];
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
+    for (int r = 0; r < R2; ++r) {
       const int t = wg + NWG * r;
       const int j = ch.j0 + t * kTileRows + lg * 32 + lane;
       posv[r] = (t < ch.ntiles && j < ch.T && (A.out.flags & kEmitKeys))
@@ -836,7 +837,7 @@ struct Epi {
     const uint32_t head_id = (uint32_t)((p.layer_id_base + ch.l) * c.kv_heads + ch.h);
     const uint32_t seq_id = (uint32_t)(p.seq_id_base + ch.s);
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
+    for (int r = 0; r < R2; ++r) {
       const int t = wg + NWG * r;
       if (t >= ch.ntiles) break;
       const int j = ch.j0 + t * kTileRows + row;
