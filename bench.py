@@ -8,8 +8,11 @@ in-place compaction) on the GB300, through the library's C ABI.
 One step = nexus_evict_step over every slice of the workload's step-0 cache (for the
 default workload: one Llama-3-8B-shaped layer, 8 KV heads x 8192 cached rows, evicted
 to 1638 rows each). Before each timed step, untimed: the cache is restored from a
-pristine device copy and a buffer twice the L2 size is written, so every step reads
-the cache from HBM. Rank 0 prints one JSON line.
+pristine device copy, a buffer twice the L2 size is written and another one as large is
+read (L2 then holds neither the cache nor dirty lines), and a sleep kernel keeps the
+device busy while the host issues the step. By default the timed loop replays one
+CUDA-graph capture of the nexus_evict_step call (--launch eager calls it every step; its
+times are reported beside). Rank 0 prints one JSON line.
 
 value   KV rows scored+evicted per second (a row = one cached token of one KV head of
         one layer), all ranks, device-timed with CUDA events on the launching stream.
@@ -17,7 +20,8 @@ e2e     the same metric end to end through the C ABI with host buffers: per step
         cache, queries and lengths are copied from pinned host memory to the device,
         the step runs, and the kept-slot lists and lengths are copied back.
 roofline  the dominant kernel: algorithmic bytes per launch / its mean event-timed
-        duration, against the measured HBM copy bandwidth.
+        duration, against the measured HBM copy bandwidth; traffic from the counter
+        capture recorded under profiles/ while the kernel's source is unchanged.
 cpu_baseline  the CPU oracle (C, OpenMP over slices) on the host cores, bounded sample.
 --impl reference  runs the CPU oracle itself as the reference arm.
 """

@@ -72,19 +72,12 @@ WsLayout layout_of(const nx_cache* c, const nx_params* p) {
   o += align_up((size_t)L.slices * 8, 256);
   L.tile_flags = o;
   o += align_up((size_t)L.slices * L.tiles_per_slice * 4, 256);
-  L.groups_per_slice = (L.max_chunks + 15) / 16;
-  L.group_arrive = o;
-  o += align_up((size_t)L.slices * L.groups_per_slice * 4, 256);
   L.counters_bytes = o - L.counters;
   const size_t cells = (size_t)L.slices * c->capacity;
   L.keys = o;
   o += align_up(cells * 4, 256);
   L.stats = o;
   o += align_up((size_t)L.slices * L.max_chunks * L.stats_stride * 4, 256);
-  L.group_rec = o;
-  o += align_up((size_t)L.slices * L.groups_per_slice * L.stats_stride * 4, 256);
-  L.fin = o;
-  o += align_up((size_t)L.slices * (3 * p->window + kMaxWalk) * 4, 256);
   L.qbar = o;
   o += align_up((size_t)L.slices * p->window * c->head_dim * 4, 256);
   L.newlen = o;

@@ -30,13 +30,9 @@ struct WsLayout {
   size_t counters_bytes;
   size_t tile_flags;     // int32 [slices][tiles_per_slice]  (inside counters)
   size_t work;           // int32 [8] global work counters     (inside counters)
-  size_t barriers;       // int32 [2][slices] slice arrivals, ready flags (inside counters)
+  size_t barriers;       // int32 [2][slices] slice arrival counts (inside counters)
   size_t keys;           // uint32 [slices][capacity] order keys
   size_t stats;          // float [slices][max_chunks][stats_stride] partial softmax stats
-  size_t fin;            // float [slices][3W + kMaxWalk] merged per-slice coefficients
-  size_t group_arrive;   // int32 [slices][groups_per_slice] (inside counters)
-  size_t group_rec;      // float [slices][groups_per_slice][stats_stride]
-  int groups_per_slice;  // chunk records are merged 16 at a time
   size_t qbar;           // float [slices][W][head_dim] group-mean window queries, or the
                          // tensor-core scorer's bf16 hi/lo image of the same size
   size_t newlen;         // int32 [slices]

@@ -12,13 +12,13 @@
 //      bf16(Qbar - bf16(Qbar)), accumulating in the same TMEM columns, so the logits keep
 //      fp32 accuracy although the tensor cores take bf16 operands. A chunk's logits fill
 //      one of two or three TMEM buffers (tile t -> columns [t*W, (t+1)*W));
-//   3. the epilogue warpgroups (one TMEM lane = one row) take the chunk maxima, write
-//      e = exp((l - max_chunk)/sqrt(d)) back to TMEM, and store the chunk record (maxima,
-//      sums, the H x H Gram of the walk rows); a publisher warp makes it visible and
-//      counts it into the slice;
+//   3. the epilogue warpgroups (one TMEM lane = one row) take per-column maxima over each
+//      warp's rows, write e = exp((l - max)/sqrt(d)) back to TMEM, and store the chunk
+//      record (chunk maxima, sums, the H x H Gram of the walk rows); a publisher warp
+//      makes it visible and counts it into the slice;
 //   4. a merge warp waits (bounded) until every chunk of the slice is counted in, merges
 //      the slice's records, runs the walk recurrence (gamma_t = 1 + sum_{u<t} gamma_u
-//      <P_t, P_u>, the rank-1 form of Eq. (4)) and hands the per-row coefficients over;
+//      <P_t, P_u>, the rank-1 form of Eq. (4)) and hands the per-column weights over;
 //   5. the epilogue turns the chunk's TMEM e values into a, c~, w and the order key of
 //      every row (one chunk behind step 3, so the slice wait overlaps the next chunk).
 // K is read from HBM exactly once; nothing but one key (and optional outputs) per row
@@ -179,21 +179,7 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
       : "memory");
 }
 
-// 32 lanes x 16 / 32 columns of 32-bit TMEM words into registers (and back).
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
+// 32 lanes x 16 columns of 32-bit TMEM words into registers (and back).
 __device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t* r) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
@@ -205,17 +191,6 @@ __device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t* r) {
 }
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// 32 (or 16 when W = 16) consecutive TMEM columns of this thread's lane, one wait.
-template <int N>
-__device__ __forceinline__ void tmem_load(uint32_t taddr, float* v) {
-  uint32_t r[N];
-  tmem_ld16_nowait(taddr, r);
-  if (N == 32) tmem_ld16_nowait(taddr + 16, r + 16);
-  tmem_ld_wait();
-#pragma unroll
-  for (int i = 0; i < N; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
@@ -300,11 +275,6 @@ __device__ __forceinline__ void epi_sync(int bar_id) {
   asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "n"(Roles<NWG>::kEpiThreads) : "memory");
 }
 
-__device__ __forceinline__ float warp_max(float x) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-  return x;
-}
 // Warp maximum of a float through its monotone integer image (one redux instruction).
 __device__ __forceinline__ float warp_max_redux(float x) {
   uint32_t b = __float_as_uint(x);
@@ -553,7 +523,6 @@ struct Epi {
   __device__ float* wca() {            // this warp's pass-2 weights
     return reinterpret_cast<float*>(sm + Smem<W, D, NWG>::kOffWca) + warp * Smem<W, D, NWG>::kWca;
   }
-  __device__ float* recs() { return reinterpret_cast<float*>(sm + Smem<W, D, NWG>::kOffRec); }
   __device__ float* apart() { return reinterpret_cast<float*>(sm + Smem<W, D, NWG>::kOffPart); }
   __device__ float* ctp() { return reinterpret_cast<float*>(sm + Smem<W, D, NWG>::kOffCt); }
   __device__ uint32_t taddr(const Chunk& ch, int t) {
@@ -566,8 +535,9 @@ struct Epi {
     return ch.j0 + (t + 1) * kTileRows <= ch.T;
   }
 
-  // Passes 1a/1b: chunk maxima, e = exp((l - max)/sqrt(d)) written back to TMEM, chunk
-  // sums and the walk-row Gram; the record goes to global memory.
+  // Passes 1a/1b: per-column maxima over this warp's rows, e = exp((l - max)/sqrt(d))
+  // written back to TMEM, sums and the walk-row Gram; the chunk's record (the four lane
+  // quarters rescaled to the chunk maxima) goes to global memory.
   template <int HT>
   __device__ void stats(const Chunk& ch) {
     constexpr int RS = Smem<W, D, NWG>::kRedStride;
@@ -716,7 +686,6 @@ struct Epi {
     }
   }
 
-  // Publish the chunk's record: count it in for its slice (thread 0, after a fence).
   // Hand the chunk's record to the publisher warp: each epilogue warp arrives once its
   // stores are issued (the arrive orders them before the publisher's fence).
   __device__ void publish(const Chunk& ch, bool ok, uint64_t* bar_pub) {
@@ -727,7 +696,8 @@ struct Epi {
     if (lane == 0) mbar_arrive(&bar_pub[ch.b]);
   }
 
-  // Wait for the slice, merge, then a, c~, w and the order key of every row.
+  // Wait for the merge warp's slice statistics, then a, c~, w and the order key of every
+  // row of the chunk.
   template <int HT>
   __device__ bool emit(const Chunk& ch) {
     using S = Smem<W, D, NWG>;
@@ -927,7 +897,8 @@ struct Epi {
 // buffer's previous user is finished and every chunk of its slice has published, pull
 // the slice's chunk records into shared memory (one bulk copy per kGroup records) and
 // merge them with an online rescale across batches: per window row the maximum and the
-// normaliser, and the walk coefficients gamma_t / (sum gamma * Z_t) of Eq. (4).
+// normaliser, and the walk coefficients gamma_t / (sum gamma * Z_t) of Eq. (4); for
+// W <= 32 it also turns them into the chunk's per-column weights.
 template <int W, int D, int NWG>
 __device__ void merge_warp(const Args& A, uint8_t* sm, int chunk_rows, int nbuf, float cl2,
                            uint64_t* bar_tempty, uint64_t* bar_mfull, uint64_t* bar_htx,
