@@ -201,6 +201,9 @@ nx_status kv_compact_noalloc(nx_cache* cache, const int32_t* keep_idx, const nx_
  * One whole eviction step: scores, walk, reservoir selection and compaction for every
  * slice, with the same results as the four calls above in sequence.
  * keep_idx_out (nullable): int32 [slices][capacity] receives the kept slots.
+ * The call only enqueues work on `stream` (a counter memset and four kernels), so it can
+ * be captured into a CUDA graph; a replay reuses the captured arguments, `step`
+ * included.
  */
 nx_status nexus_evict_step(nx_cache* cache, const void* q, const nx_params* params,
                            int32_t* keep_idx_out, void* ws, size_t ws_bytes,
