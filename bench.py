@@ -187,12 +187,26 @@ def barrier(world):
 
 
 def allmax(x: float, world: int) -> float:
+    """Maximum of x over the ranks (the slowest rank's time decides)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cpu" if dist.get_backend() == "gloo" else "cuda"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def rank_seq_base(rank: int, wl) -> int:
+    """First Philox sequence id of this rank: every rank evicts its own sequences."""
+    return rank * wl.seqs
+
+
+def job_rate(rows_per_step: int, steps: int, local_ms: float, world: int) -> tuple:
+    """Whole-job rows/s: the rows all ranks processed over the slowest rank's time.
+    Returns (rows/s, max-over-ranks milliseconds)."""
+    total_ms = allmax(local_ms, world)
+    return rows_per_step * steps * world / (total_ms / 1e3), total_ms
 
 
 # ---------------------------------------------------------------------------
@@ -234,7 +248,7 @@ def run_native(args, rank, world, local):
     params = nexus.Params(budget=work["budget"], budget_max=int(wl.budget.max()),
                           window=wl.window, walk_len=wl.walk_len, n_sink=wl.n_sink,
                           n_recent=wl.n_recent, lam=wl.lam, eps_tie=wl.eps_tie,
-                          seed=wl.philox_seed, step=0, seq_id_base=rank * wl.seqs)
+                          seed=wl.philox_seed, step=0, seq_id_base=rank_seq_base(rank, wl))
     ws = nexus.alloc_workspace(cache, params)
     status = nexus.new_status(dev)
     keep = torch.full((cache.n_slices, wl.capacity), -1, dtype=torch.int32, device=dev)
@@ -332,7 +346,7 @@ def run_native(args, rank, world, local):
     time.sleep(0.2)
     clocks = sampler.stop()
     assert int(status.item()) == 0, f"device status {int(status.item())}"
-    total_ms = allmax(sum(step_ms), world)
+    local_ms = sum(step_ms)
     eager = None
     if graph is not None:
         # the same step called eagerly through the C ABI (host launch latency included
@@ -347,7 +361,7 @@ def run_native(args, rank, world, local):
     newlen = work["lens"].reshape(-1).cpu().numpy()
     ab = algorithmic_bytes(wl, lens0, keep.cpu().numpy(), newlen)
     rows_per_step = ab["rows"]
-    value = rows_per_step * K * world / (total_ms / 1e3)
+    value, total_ms = job_rate(rows_per_step, K, local_ms, world)
 
     # dominant kernel and its roofline
     dom = max(per_kernel, key=per_kernel.get)
@@ -399,8 +413,8 @@ def run_native(args, rank, world, local):
         e_e[i].record(stream)
     torch.cuda.synchronize()
     barrier(world)
-    e2e_ms = allmax(sum(e_s[i].elapsed_time(e_e[i]) for i in range(e2e_steps)), world)
-    e2e_value = rows_per_step * e2e_steps * world / (e2e_ms / 1e3)
+    e2e_value, _ = job_rate(rows_per_step, e2e_steps,
+                            sum(e_s[i].elapsed_time(e_e[i]) for i in range(e2e_steps)), world)
 
     out = dict(metric=METRIC, value=round(value, 1), unit=UNIT, n_gpus=world, steps=K,
                warmup=args.warmup, ms_per_step=round(total_ms / K, 5), higher_is_better=True,
