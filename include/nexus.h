@@ -201,7 +201,7 @@ nx_status kv_compact_noalloc(nx_cache* cache, const int32_t* keep_idx, const nx_
  * One whole eviction step: scores, walk, reservoir selection and compaction for every
  * slice, with the same results as the four calls above in sequence.
  * keep_idx_out (nullable): int32 [slices][capacity] receives the kept slots.
- * The call only enqueues work on `stream` (a counter memset and four kernels), so it can
+ * The call only enqueues work on `stream` (four kernels), so it can
  * be captured into a CUDA graph; a replay reuses the captured arguments, `step`
  * included.
  */

@@ -180,7 +180,7 @@ nx_status nexus_direct_scores(const nx_cache* cache, const void* q, const nx_par
   if (!q || ((uintptr_t)q & 15u) || !a_out) return NX_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   char* w = static_cast<char*>(ws);
-  NX_TRY(cudaMemsetAsync(w + L.counters, 0, L.counters_bytes, st));
+  // the counters are zeroed by the first kernel (prep)
   ScoreOut out{};
   out.a = a_out;
   out.row_stats = row_stats_out;
@@ -200,7 +200,7 @@ nx_status nexus_walk(const nx_cache* cache, const void* q, const nx_params* para
   if (!q || ((uintptr_t)q & 15u) || !w_out) return NX_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   char* w = static_cast<char*>(ws);
-  NX_TRY(cudaMemsetAsync(w + L.counters, 0, L.counters_bytes, st));
+  // the counters are zeroed by the first kernel (prep)
   ScoreOut out{};
   out.w = w_out;
   out.ctilde = ctilde_out;
@@ -259,7 +259,7 @@ nx_status nexus_evict_step(nx_cache* cache, const void* q, const nx_params* para
   int32_t* newlen = reinterpret_cast<int32_t*>(w + L.newlen);
   uint32_t* keys = reinterpret_cast<uint32_t*>(w + L.keys);
   int32_t* keep = keep_idx_out ? keep_idx_out : reinterpret_cast<int32_t*>(w + L.keep);
-  NX_TRY(cudaMemsetAsync(w + L.counters, 0, L.counters_bytes, st));
+  // the counters are zeroed by the first kernel (prep)
   ScoreOut out{};
   out.keys = keys;
   out.flags = kEmitKeys;

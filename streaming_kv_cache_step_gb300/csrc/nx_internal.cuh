@@ -224,7 +224,8 @@ cudaError_t launch_after(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t
 // nx_score.cu
 cudaError_t launch_prep(const nx_cache& c, const void* q, const nx_params& p, const WsLayout& L,
                         char* ws, int32_t* dev_status, cudaStream_t st, int* launches,
-                        int mode);   // 0: validity only, 1: fp32 Qbar, 2: tensor-core image
+                        int mode);   // 0: validity only, 1: fp32 Qbar, 2: tensor-core image;
+                                     // also zeroes the workspace counters
 // nx_score_tc.cu: *used is false when the shape is not covered (the caller falls back)
 bool tc_supported(const nx_cache& c, const nx_params& p);
 void tc_set_trace(long long* buf);

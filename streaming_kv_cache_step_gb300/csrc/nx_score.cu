@@ -35,7 +35,17 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4 raw, float* out) {
 // Grid: (slices, W); one thread per pair of adjacent features.
 __global__ void prep_kernel(nx_cache c, const void* __restrict__ q, nx_params p,
                             void* __restrict__ qout, int32_t* __restrict__ newlen,
-                            int32_t* dev_status, int mode) {
+                            int32_t* dev_status, int mode, int4* __restrict__ counters,
+                            long long counter_vecs) {
+  // the step's counters (slice arrivals, compaction claims and flags) start at zero; the
+  // kernels that use them run after this one
+  {
+    const long long n = (long long)gridDim.x * gridDim.y * blockDim.x;
+    for (long long i = ((long long)blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x +
+                       threadIdx.x;
+         i < counter_vecs; i += n)
+      counters[i] = make_int4(0, 0, 0, 0);
+  }
   const int slice = blockIdx.x;
   int l, s, h;
   slice_coords(c, slice, l, s, h);
@@ -349,8 +359,11 @@ cudaError_t launch_prep(const nx_cache& c, const void* q, const nx_params& p, co
                         char* ws, int32_t* dev_status, cudaStream_t st, int* launches,
                         int mode) {
   dim3 grid((unsigned)L.slices, mode == 0 ? 1 : p.window);
+  // counters_bytes is a multiple of 64 and the region 256-byte aligned
   prep_kernel<<<grid, 64, 0, st>>>(c, q, p, ws + L.qbar,
-                                   reinterpret_cast<int32_t*>(ws + L.newlen), dev_status, mode);
+                                   reinterpret_cast<int32_t*>(ws + L.newlen), dev_status, mode,
+                                   reinterpret_cast<int4*>(ws + L.counters),
+                                   (long long)(L.counters_bytes / 16));
   note_launch(st, launches, "prep");
   return cudaGetLastError();
 }
