@@ -3,11 +3,12 @@
 in-place compaction) on the GB300, through the library's C ABI.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
-                    [--workload llama3_8b_layer]
+                    [--workload batch16_32layers]
 
 One step = nexus_evict_step over every slice of the workload's step-0 cache (for the
-default workload: one Llama-3-8B-shaped layer, 8 KV heads x 8192 cached rows, evicted
-to 1638 rows each). Before each timed step, untimed: the cache is restored from a
+default workload: 16 sequences x 32 layers x 8 KV heads of 32768 cached rows each, d =
+128 bf16, evicted to 6554 rows each -- 134M rows, 68.7 GB of K and V, the largest
+single-GPU workload). Before each timed step, untimed: the cache is restored from a
 pristine device copy, a buffer twice the L2 size is written and another one as large is
 read (L2 then holds neither the cache nor dirty lines), and a sleep kernel keeps the
 device busy while the host issues the step. By default the timed loop replays one
@@ -22,7 +23,7 @@ e2e     the same metric end to end through the C ABI with host buffers: per step
 roofline  the dominant kernel: algorithmic bytes per launch / its mean event-timed
         duration, against the measured HBM copy bandwidth; traffic from the counter
         capture recorded under profiles/ while the kernel's source is unchanged.
-cpu_baseline  the CPU oracle (C, OpenMP over slices) on the host cores, bounded sample.
+cpu_baseline  the CPU oracle (C) on every host core (one slice per thread), bounded sample.
 --impl reference  runs the CPU oracle itself as the reference arm.
 """
 from __future__ import annotations
@@ -54,7 +55,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("native", "reference"), default="native")
-    ap.add_argument("--workload", default="llama3_8b_layer")
+    ap.add_argument("--workload", default="batch16_32layers")
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--launch", choices=("graph", "eager"), default="graph",
@@ -233,15 +234,25 @@ def algorithmic_bytes(wl, lens0: np.ndarray, keep: np.ndarray, newlen: np.ndarra
 # native arm
 # ---------------------------------------------------------------------------
 
+_T0 = time.time()
+
+
+def _log(msg: str) -> None:
+    """Progress of the set-up phases on stderr (stdout carries only the JSON line)."""
+    print(f"[bench {time.time() - _T0:7.1f} s] {msg}", file=sys.stderr, flush=True)
+
+
 def run_native(args, rank, world, local):
     from streaming_kv_cache_step_gb300 import nexus
     from streaming_kv_cache_step_gb300 import workloads as W
     import __graft_entry__
     __graft_entry__.build()
+    _log("library built and loaded")
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     wl = W.WORKLOADS[args.workload]()
     pristine = W.make_cache(wl, dev)
+    _log(f"cache of {wl.name} generated on the device")
     work = {k: (v.clone() if torch.is_tensor(v) else v) for k, v in pristine.items()}
     q = W.queries(wl, 0, dev)
     cache = nexus.Cache.from_dict(work)
@@ -334,6 +345,7 @@ def run_native(args, rank, world, local):
         torch.cuda.synchronize()
         assert int(status.item()) == 0, f"device status {int(status.item())}"
 
+    _log("warm-up done")
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
@@ -356,6 +368,7 @@ def run_native(args, rank, world, local):
         eager = dict(ms_per_step=round(allmax(sum(e_ms), world) / ke, 5), steps=ke,
                      kernels_us={k: round(v, 3) for k, v in e_kern.items()})
 
+    _log("timed loops done")
     # algorithmic bytes of this step (from the kept-slot lists of the last step)
     lens0 = pristine["lens"].reshape(-1).cpu().numpy()
     newlen = work["lens"].reshape(-1).cpu().numpy()
@@ -385,7 +398,9 @@ def run_native(args, rank, world, local):
                                     alg_bytes=ab["total"]))
 
     # ---- end to end through the C ABI with host buffers ----
-    e2e_steps = args.e2e_steps or max(3, min(K, 50))
+    # about 1e11 bytes of host->device copies at most (five steps of the 68.7 GB cache)
+    cache_bytes = sum(pristine[n].numel() * pristine[n].element_size() for n in names)
+    e2e_steps = args.e2e_steps or max(3, min(K, 50, int(4e11 // max(cache_bytes, 1))))
     host = {n: torch.empty_like(pristine[n], device="cpu").pin_memory() for n in names}
     for n in names:
         host[n].copy_(pristine[n])
@@ -413,6 +428,7 @@ def run_native(args, rank, world, local):
         e_e[i].record(stream)
     torch.cuda.synchronize()
     barrier(world)
+    _log(f"end-to-end loop done ({e2e_steps} steps)")
     e2e_value, _ = job_rate(rows_per_step, e2e_steps,
                             sum(e_s[i].elapsed_time(e_e[i]) for i in range(e2e_steps)), world)
 
@@ -445,9 +461,12 @@ def run_native(args, rank, world, local):
 # CPU oracle (cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
 
-def _oracle_slices(wl, max_slices):
+def _oracle_slices(wl, n):
+    """n sampled step-0 slices of the workload (one per host thread); a workload with
+    fewer slices than threads repeats them, so that every core has a slice to score."""
     from streaming_kv_cache_step_gb300 import workloads as W
-    return [W.slice_numpy_cache(wl, sid) for sid in range(min(wl.n_slices, max_slices))]
+    made = [W.slice_numpy_cache(wl, sid) for sid in range(min(wl.n_slices, n))]
+    return [made[i % len(made)] for i in range(n)]
 
 
 def _oracle_pass(wl, slices, pool):
@@ -474,6 +493,7 @@ def oracle_rate(wl, budget_s: float):
     oracle.build()
     cores = os.cpu_count() or 1
     slices = _oracle_slices(wl, cores)
+    distinct = min(wl.n_slices, cores)
     rows, passes = 0, 0
     with ThreadPoolExecutor(max_workers=len(slices)) as pool:
         t0 = time.perf_counter()
@@ -483,9 +503,11 @@ def oracle_rate(wl, budget_s: float):
             dt = time.perf_counter() - t0
             if dt >= budget_s:
                 break
-    return dict(value=round(rows / dt, 1), unit=UNIT, cores=len(slices), kind="oracle",
-                sample=f"{passes} passes over {len(slices)} of the {wl.n_slices} step-0 slices "
-                       f"of {wl.name} ({rows} rows, {dt:.1f} s wall), one host thread per slice")
+    return dict(value=round(rows / dt, 1), unit=UNIT, cores=cores, threads=len(slices),
+                kind="oracle",
+                sample=f"{passes} passes over {len(slices)} slices ({distinct} distinct) of the "
+                       f"{wl.n_slices} step-0 slices of {wl.name} ({rows} rows, {dt:.1f} s "
+                       f"wall), one host thread per slice")
 
 
 def run_reference(args, rank, world):
@@ -498,7 +520,8 @@ def run_reference(args, rank, world):
     import oracle
     oracle.build()
     wl = W.WORKLOADS[args.workload]()
-    slices = _oracle_slices(wl, os.cpu_count() or 1)
+    cores = os.cpu_count() or 1
+    slices = _oracle_slices(wl, cores)
     with ThreadPoolExecutor(max_workers=len(slices)) as pool:
         for _ in range(args.warmup):
             _oracle_pass(wl, slices, pool)
@@ -508,8 +531,8 @@ def run_reference(args, rank, world):
             rows += _oracle_pass(wl, slices, pool)
         dt = time.perf_counter() - t0
     value = rows / dt
-    sample = (f"{len(slices)} of the {wl.n_slices} step-0 slices of {wl.name} per step, "
-              f"one host thread per slice")
+    sample = (f"{len(slices)} slices ({min(wl.n_slices, cores)} distinct) of the "
+              f"{wl.n_slices} step-0 slices of {wl.name} per step, one host thread per slice")
     return dict(metric=METRIC, value=round(value, 1), unit=UNIT, n_gpus=world,
                 steps=args.steps, warmup=args.warmup,
                 ms_per_step=round(dt / max(args.steps, 1) * 1e3, 3), higher_is_better=True,
@@ -517,8 +540,8 @@ def run_reference(args, rank, world):
                 impl="reference",
                 config=dict(workload=wl.name, sample_slices=len(slices),
                             rows_per_step=rows // max(args.steps, 1)),
-                cpu_baseline=dict(value=round(value, 1), unit=UNIT, cores=len(slices),
-                                  kind="oracle", sample=sample),
+                cpu_baseline=dict(value=round(value, 1), unit=UNIT, cores=cores,
+                                  threads=len(slices), kind="oracle", sample=sample),
                 e2e=dict(value=round(value, 1), unit=UNIT, h2d_bytes_per_step=0,
                          d2h_bytes_per_step=0))
 
@@ -535,6 +558,7 @@ def main():
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
             out["cpu_baseline"] = oracle_rate(wl, budget_s=10.0)
+            _log("cpu baseline done")
         print(json.dumps(out), flush=True)
     if world > 1:
         import torch.distributed as dist

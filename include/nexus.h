@@ -189,10 +189,14 @@ nx_status kv_compact(nx_cache* cache, const int32_t* keep_idx, const nx_params* 
  * up to 256) + 4 * slices * ceil(budget_max / 32) (rounded up to 256) bytes must fit
  * in 4 MiB; larger calls return NX_ERR_WORKSPACE without launching anything. The
  * function calls no cudaMalloc, cudaFree or other allocating routine.
- * The first call on each device looks up the array's device address (with that
- * device current) and must come before any stream capture that includes it. All calls
- * share the one array: calls that overlap on the GPU (other streams, other host
- * threads) race and must be serialised by the caller.
+ * Every call made outside a stream capture looks up the array's device address for the
+ * current device (a host-side query that allocates nothing) and remembers it; a call
+ * made while its stream is being captured uses the remembered address, so the first
+ * call on each device must come before any capture that includes this function (after
+ * cudaDeviceReset, make one uncaptured call again). All calls share the one array,
+ * which keeps the previous call's contents until the next call clears what must start
+ * at zero: calls that overlap on the GPU (other streams, other host threads) race and
+ * must be serialised by the caller.
  */
 nx_status kv_compact_noalloc(nx_cache* cache, const int32_t* keep_idx, const nx_params* params,
                              int32_t* dev_status, nx_stream_t stream);
@@ -253,6 +257,19 @@ void nexus_debug_scorer_config(int32_t* out8);
 
 /* Static, human-readable name of a status code. */
 const char* nx_status_string(nx_status status);
+
+/*
+ * Which scorer the most recent entry-point call made from this host thread used for the
+ * direct scores and the walk (not part of the method; lets a caller see a fallback):
+ *   NX_SCORER_NONE         the call computed no scores (selection or compaction only, or
+ *                          it was rejected before launching anything);
+ *   NX_SCORER_TENSOR_CORE  the tcgen05 scorer, which reads every cached key once;
+ *   NX_SCORER_CUDA_CORE    the CUDA-core scorer (fp32 caches, shapes the tensor-core
+ *                          scorer does not cover), which reads every cached key twice.
+ * The results are the same within the score tolerance either way.
+ */
+enum { NX_SCORER_NONE = 0, NX_SCORER_TENSOR_CORE = 1, NX_SCORER_CUDA_CORE = 2 };
+int32_t nexus_last_scorer(void);
 
 /* Kernels launched by the most recent call made from this host thread. */
 int32_t nexus_last_launch_count(void);

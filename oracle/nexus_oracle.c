@@ -22,7 +22,8 @@
  *   Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3"
  *     (SC'11): the Philox4x32 bijection with 10 rounds.
  *
- * Readings where the text is open (each one is listed in the design notes):
+ * Readings where §2.1-§2.3 leave a detail unstated (each the plainest reading of the
+ * surrounding text):
  *   block size b = 1 (BlockSum and rownorm are identities); the window query Q
  *   is the mean of the G query heads that share the KV head; no causal mask;
  *   the walk uses the last H window rows oldest first, without damping, and

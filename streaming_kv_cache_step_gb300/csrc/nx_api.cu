@@ -3,13 +3,16 @@
 #include <math.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "nx_internal.cuh"
 
 namespace nx {
 namespace {
 
 thread_local int32_t g_last_launches = 0;
-bool g_force_simt = false;    // set by nexus_debug_force_simt (tests, comparisons)
+thread_local int32_t g_last_scorer = NX_SCORER_NONE;
+std::atomic<bool> g_force_simt{false};   // set by nexus_debug_force_simt (tests, comparisons)
 constexpr int kMaxLaunchNames = 16;
 thread_local const char* g_launch_names[kMaxLaunchNames];
 thread_local void* const* g_prof_events = nullptr;   // armed by nexus_profile_next_call
@@ -99,6 +102,8 @@ nx_status common_checks(const nx_cache* c, const nx_params* p, void* ws, size_t 
   return NX_OK;
 }
 
+}  // namespace
+
 nx_status finish(cudaError_t e, int launches) {
   g_last_launches = launches;
   if (g_prof_active) {
@@ -108,6 +113,15 @@ nx_status finish(cudaError_t e, int launches) {
   }
   return e == cudaSuccess ? NX_OK : NX_ERR_CUDA;
 }
+
+// Called at the start of every entry point: consumes an armed profiling request.
+void begin_call() {
+  g_last_launches = 0;
+  g_last_scorer = NX_SCORER_NONE;
+  g_prof_active = g_prof_events != nullptr;
+}
+
+namespace {
 
 #define NX_TRY(expr)                         \
   do {                                       \
@@ -120,24 +134,23 @@ nx_status finish(cudaError_t e, int launches) {
 cudaError_t run_scores(const nx_cache& c, const void* q, const nx_params& p, const WsLayout& L,
                        char* ws, const ScoreOut& out, int32_t* dev_status, cudaStream_t st,
                        int* launches) {
-  const bool tc = tc_supported(c, p) && !g_force_simt;
+  const bool tc = tc_supported(c, p) && !g_force_simt.load(std::memory_order_relaxed);
   cudaError_t e = launch_prep(c, q, p, L, ws, dev_status, st, launches, tc ? 2 : 1);
   if (e != cudaSuccess) return e;
   if (tc) {
     bool used = false;
     e = launch_score_tc(c, p, q, L, ws, out, dev_status, st, launches, &used);
-    if (e != cudaSuccess || used) return e;
+    if (e != cudaSuccess) return e;
+    if (used) {
+      g_last_scorer = NX_SCORER_TENSOR_CORE;
+      return e;
+    }
     // not launchable for this size: the CUDA-core path needs the fp32 queries
     e = launch_prep(c, q, p, L, ws, dev_status, st, launches, 1);
     if (e != cudaSuccess) return e;
   }
+  g_last_scorer = NX_SCORER_CUDA_CORE;
   return launch_score_simt(c, p, L, ws, out, dev_status, st, launches);
-}
-
-// Called at the start of every entry point: consumes an armed profiling request.
-void begin_call() {
-  g_last_launches = 0;
-  g_prof_active = g_prof_events != nullptr;
 }
 
 }  // namespace
@@ -303,7 +316,9 @@ const char* nx_status_string(nx_status status) {
 
 int32_t nexus_last_launch_count(void) { return g_last_launches; }
 
-void nexus_debug_force_simt(int32_t on) { g_force_simt = on != 0; }
+int32_t nexus_last_scorer(void) { return g_last_scorer; }
+
+void nexus_debug_force_simt(int32_t on) { g_force_simt.store(on != 0); }
 
 void nexus_debug_scorer_layout(int32_t teams) {
   nx::tc_set_layout(teams == 1 || teams == 2 ? teams : 0);

@@ -178,6 +178,10 @@ __device__ __forceinline__ bool wait_at_least(const int* addr, int target, int32
 // Bookkeeping after every kernel launch of an entry point: counts it, remembers its
 // name and, when a benchmark armed nexus_profile_next_call, records its event.
 void note_launch(cudaStream_t st, int* launches, const char* name);
+// Every entry point calls begin_call() first and returns through finish() once it has
+// enqueued its kernels (launch count and names, the profiling request, the status).
+void begin_call();
+nx_status finish(cudaError_t e, int launches);
 
 // ---------------------------------------------------------------------------
 // Kernel launchers (one per source file)

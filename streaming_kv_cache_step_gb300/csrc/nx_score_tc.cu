@@ -26,6 +26,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
+
 #include "nx_internal.cuh"
 
 namespace nx {
@@ -1264,8 +1266,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
-long long* g_trace = nullptr;     // installed by nexus_debug_set_trace
-int g_layout = 0;                 // pipelines per CTA asked for (0: automatic)
+std::atomic<long long*> g_trace{nullptr};   // installed by nexus_debug_set_trace
+std::atomic<int> g_layout{0};               // pipelines per CTA asked for (0: automatic)
 thread_local int32_t g_last_cfg[8];
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1313,9 +1315,11 @@ cudaError_t launch_t(const nx_cache& c, const nx_params& p, const void* q, const
   if (L.stats_stride != S::kRecStride) { g_last_cfg[0] = -2; return cudaSuccess; }
   int dev = 0, sms = 0, per_sm_api = 0;
   cudaGetDevice(&dev);
-  static bool attr_set[64] = {};
+  // per device and instantiation; setting the attributes twice (two host threads racing
+  // on the first call) is harmless
+  static std::atomic<bool> attr_set[64];
   if (dev < 0 || dev >= 64) return cudaSuccess;
-  if (!attr_set[dev]) {
+  if (!attr_set[dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(score_tc_kernel<W, D, NWG>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, S::kAlloc);
     if (e != cudaSuccess) return e;
@@ -1323,7 +1327,7 @@ cudaError_t launch_t(const nx_cache& c, const nx_params& p, const void* q, const
                              cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_api, score_tc_kernel<W, D, NWG>,
@@ -1396,7 +1400,7 @@ cudaError_t launch_t(const nx_cache& c, const nx_params& p, const void* q, const
     a.stride = L.stats_stride;
     a.total_ids = slices * maxc;
     a.slices = (int)slices;
-    a.trace = g_trace;
+    a.trace = g_trace.load(std::memory_order_relaxed);
     const long long vgrid = a.total_ids < grid_sel ? a.total_ids : grid_sel;
     const long long grid = (vgrid + R::kTeams - 1) / R::kTeams;  // CTAs of kTeams teams
 
@@ -1443,8 +1447,8 @@ cudaError_t launch_t(const nx_cache& c, const nx_params& p, const void* q, const
 
 }  // namespace tc
 
-void tc_set_trace(long long* buf) { tc::g_trace = buf; }
-void tc_set_layout(int teams) { tc::g_layout = teams; }
+void tc_set_trace(long long* buf) { tc::g_trace.store(buf); }
+void tc_set_layout(int teams) { tc::g_layout.store(teams); }
 void tc_last_config(int32_t* out) {
   for (int i = 0; i < 8; ++i) out[i] = tc::g_last_cfg[i];
 }
@@ -1474,10 +1478,11 @@ cudaError_t launch_score_tc(const nx_cache& c, const nx_params& p, const void* q
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const bool big = rows_all >= 8LL * 512 * (sms > 0 ? sms : 1) && c.page_size > 0;
-  if (p.window <= 32 && (tc::g_layout == 2 || (tc::g_layout == 0 && big))) {
+  const int layout = tc::g_layout.load(std::memory_order_relaxed);
+  if (p.window <= 32 && (layout == 2 || (layout == 0 && big))) {
     cudaError_t e = p.window == 16 ? (d128 ? NX_TC_LAUNCH(16, 128, 2) : NX_TC_LAUNCH(16, 64, 2))
                                    : (d128 ? NX_TC_LAUNCH(32, 128, 2) : NX_TC_LAUNCH(32, 64, 2));
-    if (e != cudaSuccess || *used || tc::g_layout == 2) return e;
+    if (e != cudaSuccess || *used || layout == 2) return e;
   }
   switch (p.window) {
     case 16: return d128 ? NX_TC_LAUNCH(16, 128, 4) : NX_TC_LAUNCH(16, 64, 4);

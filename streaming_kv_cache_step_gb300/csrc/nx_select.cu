@@ -7,6 +7,8 @@
 // largest composite by an MSB-first radix select (four 8-bit digit passes on the key,
 // four more on the slot only when the threshold key is tied), then writes the kept
 // slots in ascending order (per-warp runs, ballots, one scan of the warp totals).
+#include <atomic>
+
 #include "nx_internal.cuh"
 
 namespace nx {
@@ -262,13 +264,13 @@ cudaError_t launch_select(const nx_cache& c, const uint32_t* keys, int32_t* keep
     const size_t bytes = (size_t)c.capacity * 4;
     int dev = 0;
     cudaGetDevice(&dev);
-    static bool attr_set[64] = {};
-    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    static std::atomic<bool> attr_set[64];   // a racing second set is harmless
+    if (dev >= 0 && dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
       cudaError_t e = cudaFuncSetAttribute(select_kernel<true>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            kSmemKeys * 4);
       if (e != cudaSuccess) return e;
-      attr_set[dev] = true;
+      attr_set[dev].store(true, std::memory_order_release);
     }
     const cudaError_t e = launch_after(select_kernel<true>, dim3((unsigned)slices),
                                        dim3(kSelThreads), bytes, st, c, keys, keep, newlen);

@@ -28,7 +28,9 @@ SYMBOLS = ("nexus_workspace_bytes", "nexus_direct_scores", "nexus_walk",
            "nexus_reservoir_select", "kv_compact", "nexus_evict_step", "nx_status_string",
            "nexus_last_launch_count", "nexus_debug_compact", "nexus_last_launch_name",
            "nexus_profile_next_call", "nexus_debug_force_simt", "nexus_debug_set_trace",
-           "nexus_debug_scorer_config", "nexus_debug_scorer_layout", "kv_compact_noalloc")
+           "nexus_debug_scorer_config", "nexus_debug_scorer_layout", "kv_compact_noalloc",
+           "nexus_last_scorer")
+SCORER_NONE, SCORER_TENSOR_CORE, SCORER_CUDA_CORE = 0, 1, 2
 
 
 class NexusError(RuntimeError):
@@ -81,6 +83,8 @@ def load(path: str = LIB_PATH):
             lib.nexus_debug_compact.restype = ctypes.c_int
             lib.nx_status_string.argtypes = [ctypes.c_int]
             lib.nx_status_string.restype = ctypes.c_char_p
+            lib.nexus_last_scorer.argtypes = []
+            lib.nexus_last_scorer.restype = ctypes.c_int32
             lib.nexus_last_launch_count.argtypes = []
             lib.nexus_last_launch_count.restype = ctypes.c_int32
             lib.nexus_last_launch_name.argtypes = [ctypes.c_int32]
@@ -125,6 +129,11 @@ def set_trace(buf) -> None:
 
 def status_string(status: int) -> str:
     return load().nx_status_string(int(status)).decode()
+
+
+def last_scorer() -> int:
+    """SCORER_TENSOR_CORE, SCORER_CUDA_CORE or SCORER_NONE for the last call of this thread."""
+    return int(load().nexus_last_scorer())
 
 
 def last_launch_count() -> int:

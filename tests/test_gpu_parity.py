@@ -28,6 +28,36 @@ def _cases():
         "mixture": W.shrink(W.batch16_32layers(), layers=2, seqs=2, kv_heads=2,
                             lens=np.full(2, 777, np.int32), capacity=800,
                             budget=np.full(2, 160, np.int32)),
+        # bf16 head_dim 64 on the tensor-core scorer (its 64-column K boxes, 8 stages)
+        "bf16_d64": W.shrink(W.llama3_8b_layer(), head_dim=64, seqs=2, kv_heads=2,
+                             lens=np.array([1200, 517], np.int32), capacity=1280,
+                             budget=np.array([256, 200], np.int32), n_hubs=8),
+        # page sizes other than 16: 8 (sixteen boxes per tile), 32, and 128 (one box per tile)
+        "paged_ps8": W.shrink(W.streaming_paged(3), page_size=8, lens=np.array([1300, 77, 1024],
+                              np.int32), capacity=1536, budget=np.array([260, 64, 204], np.int32)),
+        "paged_ps32": W.shrink(W.streaming_paged(3), page_size=32,
+                               lens=np.array([1500, 900, 33], np.int32), capacity=1536,
+                               budget=np.array([300, 180, 64], np.int32)),
+        "paged_ps128": W.shrink(W.streaming_paged(2), page_size=128,
+                                lens=np.array([1900, 1280], np.int32), capacity=2048,
+                                budget=np.array([380, 256], np.int32)),
+        # a capacity that is not a multiple of four (the selection's scalar key staging)
+        "cap_1023": W.shrink(W.llama3_8b_layer(), seqs=2, kv_heads=2,
+                             lens=np.array([1023, 611], np.int32), capacity=1023,
+                             budget=np.array([205, 150], np.int32), n_hubs=8),
+        # walk lengths other than 0, 3 and 5 (the generic walk epilogue)
+        "walk_h1_w16": W.shrink(W.llama3_8b_layer(), window=16, walk_len=1, seqs=1, kv_heads=2,
+                                lens=np.array([1100], np.int32), capacity=1152,
+                                budget=np.array([220], np.int32), n_hubs=8),
+        "walk_h2": W.shrink(W.llama3_8b_layer(), walk_len=2, seqs=1, kv_heads=2,
+                            lens=np.array([900], np.int32), capacity=1024,
+                            budget=np.array([180], np.int32), n_hubs=8),
+        "walk_h4": W.shrink(W.llama3_8b_layer(), walk_len=4, seqs=2, kv_heads=1,
+                            lens=np.array([1000, 700], np.int32), capacity=1024,
+                            budget=np.array([200, 140], np.int32), n_hubs=8),
+        "walk_h4_w16": W.shrink(W.llama3_8b_layer(), window=16, walk_len=4, seqs=1,
+                                kv_heads=2, lens=np.array([800], np.int32), capacity=896,
+                                budget=np.array([160], np.int32), n_hubs=8),
     }
 
 
@@ -53,9 +83,13 @@ def _layout_case(name, lay):
     return wl
 
 
-def _check_layout_used(lay):
+def _check_layout_used(lay, wl=None):
     if lay == 2:
         assert nexus.scorer_config()["teams_per_cta"] == 2, nexus.scorer_config()
+    if wl is not None:
+        # bf16 caches run on the tensor-core scorer, fp32 ones on the CUDA-core scorer
+        want = nexus.SCORER_TENSOR_CORE if wl.dtype == "bf16" else nexus.SCORER_CUDA_CORE
+        assert nexus.last_scorer() == want, (nexus.last_scorer(), nexus.scorer_config())
 
 
 def _decode(c, q, wl):
@@ -82,7 +116,7 @@ def test_scores_and_walk_match_oracle(name, layout):
     nexus.direct_scores(run.cache, run.q, run.params, a, stats, run.ws, run.status)
     nexus.walk(run.cache, run.q, run.params, w, ct, run.ws, run.status)
     run.check_status()
-    _check_layout_used(layout)
+    _check_layout_used(layout, wl)
     a, stats, w, ct = a.cpu().numpy(), stats.cpu().numpy(), w.cpu().numpy(), ct.cpu().numpy()
     lens = run.lens()
     for sid in range(S):
@@ -158,7 +192,7 @@ def test_evict_step_end_to_end(name, layout):
     lens0 = run.lens()
     nexus.evict_step(run.cache, run.q, run.params, run.keep, run.ws, run.status)
     run.check_status()
-    _check_layout_used(layout)
+    _check_layout_used(layout, wl)
     keep = run.keep.cpu().numpy()
     lens = run.lens()
     for sid in range(S):
@@ -247,7 +281,8 @@ def test_bounded_wait_times_out_and_context_survives():
     assert run2.lens()[0] == 1638
 
 
-@pytest.mark.parametrize("name", ["gqa_ragged", "paged", "long_w64_h5", "mixture"])
+@pytest.mark.parametrize("name", ["gqa_ragged", "paged", "long_w64_h5", "mixture", "bf16_d64",
+                                  "walk_h4"])
 def test_tensor_core_scorer_matches_cuda_core_scorer(name):
     # the bf16 shapes run on the tcgen05 scorer by default; the CUDA-core scorer is an
     # independent kernel on the same inputs: both must agree within the score tolerance
@@ -329,7 +364,7 @@ def test_degenerate_lengths_end_to_end(layout):
     w = w.cpu().numpy()
     nexus.evict_step(run.cache, run.q, run.params, run.keep, run.ws, run.status)
     run.check_status()
-    _check_layout_used(layout)
+    _check_layout_used(layout, wl)
     keep = run.keep.cpu().numpy()
     lens = run.lens()
     for sid in range(S):
@@ -344,3 +379,84 @@ def test_degenerate_lengths_end_to_end(layout):
             for name_ in ("k", "v", "pos"):
                 got = W.storage_to_numpy(run.slice_rows(name_, sid, nl))
                 assert np.array_equal(got, c[name_][0, 0, 0][keep[sid, :nl]]), (sid, name_)
+
+
+def _select_on_given_weights(wl, w_np, mode):
+    """nexus_reservoir_select on caller-given weights against the oracle's select_slice,
+    slice by slice (bit-exact)."""
+    run = GpuRun(wl, mode=mode)
+    S, cap = run.cache.n_slices, wl.capacity
+    w_in = torch.zeros((S, cap), device=DEV)
+    lens = run.lens()
+    for sid in range(S):
+        T = int(lens[sid])
+        w_in[sid, :T] = torch.as_tensor(w_np[sid, :T], device=DEV)
+    nexus.reservoir_select(w_in, run.cache, run.params, run.keep, run.ws, run.status)
+    run.check_status()
+    keep = run.keep.cpu().numpy()
+    for sid in range(S):
+        layer, s, h = wl.slice_coords(sid)
+        T = int(lens[sid])
+        pos = np.arange(T, dtype=np.int32)      # step-0 caches hold position j at slot j
+        ref, _ = oracle.select_slice(w_np[sid, :T], pos, int(wl.budget[s]), wl.n_sink,
+                                     wl.n_recent, mode, wl.philox_seed, 0,
+                                     layer * wl.kv_heads + h, s)
+        assert np.array_equal(keep[sid, :ref.size], ref), sid
+        assert (keep[sid, ref.size:] == -1).all()
+
+
+TIES = W.shrink(W.llama3_8b_layer(), seqs=3, kv_heads=2,
+                lens=np.array([3000, 1999, 640], np.int32), capacity=3072,
+                budget=np.array([600, 400, 128], np.int32), n_hubs=4)
+
+
+def test_select_topk_heavily_tied_weights_bitexact():
+    # weights on a grid of 20 values: the threshold key is tied many times over, so the
+    # selection resolves the cutoff by the slot passes (the newer slot wins)
+    rng = np.random.default_rng(21)
+    S, cap = TIES.n_slices, TIES.capacity
+    w = (rng.integers(0, 20, (S, cap)) / 7).astype(np.float32)
+    _select_on_given_weights(TIES, w, nexus.MODE_TOPK)
+
+
+def test_select_reservoir_with_zero_weights_bitexact():
+    # zero weights give the key ln(u)/0 = -inf: when fewer positive-weight candidates
+    # remain than the budget asks for, the -inf keys tie at the cutoff
+    rng = np.random.default_rng(22)
+    S, cap = TIES.n_slices, TIES.capacity
+    w = rng.random((S, cap)).astype(np.float32) * 1e-3
+    lens = TIES.lens
+    for sid in range(S):
+        s = TIES.slice_coords(sid)[1]
+        T, B = int(lens[s]), int(TIES.budget[s])
+        zero = rng.choice(np.arange(32, T - 32), T - 64 - (B - 64) // 2, replace=False)
+        w[sid, zero] = 0.0      # only (B - 64) / 2 candidates keep a positive weight
+    _select_on_given_weights(TIES, w, nexus.MODE_RESERVOIR)
+
+
+def test_slice_beyond_the_tensor_core_residency_limit():
+    # One slice longer than the tensor-core scorer's co-resident chunks hold (152 pipelines
+    # x 8 tiles x 128 rows): the call still gives the oracle's results, and reports which
+    # scorer it used.
+    T = 160_000
+    wl = W.shrink(W.llama3_8b_layer(), seqs=1, kv_heads=1, lens=np.array([T], np.int32),
+                  capacity=T, budget=np.array([T // 5], np.int32), n_hubs=16)
+    run = GpuRun(wl)
+    w = torch.full((1, T), -1.0, device=DEV)
+    nexus.walk(run.cache, run.q, run.params, w, None, run.ws, run.status)
+    run.check_status()
+    scorer = nexus.last_scorer()
+    assert scorer in (nexus.SCORER_TENSOR_CORE, nexus.SCORER_CUDA_CORE)
+    print("scorer", scorer, nexus.scorer_config())
+    nexus.evict_step(run.cache, run.q, run.params, run.keep, run.ws, run.status)
+    run.check_status()
+    assert nexus.last_scorer() == scorer
+    c, _, _, ref = oracle_slice(wl, 0)
+    w = w.cpu().numpy()
+    assert np.all(np.abs(w[0] - ref["w"][0, :T]) <= score_tol(ref["w"][0, :T], T))
+    nl = int(ref["newlen"][0])
+    kappa = oracle_kappa(wl, 0, ref["w"][0, :T], c["pos"][0, 0, 0, :T])
+    keep = run.keep.cpu().numpy()
+    compare_survivors(keep[0, :nl], ref["keep"][0, :nl], kappa)
+    got = W.storage_to_numpy(run.slice_rows("k", 0, nl))
+    assert np.array_equal(got, c["k"][0, 0, 0][keep[0, :nl]])
