@@ -67,30 +67,14 @@ static double nxo_load(const void* base, int dtype, int64_t idx) {
 /* ------------------------------------------------------------------------ */
 
 /*
- * K: T x d rows of cached keys; Qbar: W x d window queries (already averaged
- * over the query heads of the group). All outputs are optional (NULL skips);
- * P (W x T) is the per-row distribution a^(q) of Eq. (3).
- *
- * Returns 0 on success, -1 on bad sizes or allocation failure.
+ * Eq. (1), the part before BlockSum: for every window row w, the logits
+ * Q_w . K_j / sqrt(D) over the whole cache (no mask) and their softmax, into
+ * P (W x T, row-major). rowmax / rowsum (optional) receive each row's maximum
+ * logit and sum of exp(logit - max).
  */
-int nxo_slice_scores(int T, int d, int W, int H, double lambda, double eps_tie,
-                     const double* K, const double* Qbar, double* P_out,
-                     double* a, double* ctilde, double* s, float* w32,
-                     double* rowmax, double* rowsum, double* gamma) {
-  if (T < 1 || d < 1 || W < 1 || H < 0 || H > W) return -1;
-  double* P = P_out ? P_out : (double*)malloc(sizeof(double) * (size_t)W * T);
-  double* C = (double*)calloc((size_t)T, sizeof(double));
-  double* ab = (double*)malloc(sizeof(double) * (size_t)T);
-  double* cb = (double*)malloc(sizeof(double) * (size_t)T);
-  if (!P || !C || !ab || !cb) {
-    if (!P_out) free(P);
-    free(C); free(ab); free(cb);
-    return -1;
-  }
+static void nxo_softmax_rows(int T, int d, int W, const double* K, const double* Qbar,
+                             double* P, double* rowmax, double* rowsum) {
   const double scale = 1.0 / sqrt((double)d);
-
-  /* Eq. (1) at b = 1: logits Q K^T / sqrt(D), then a softmax over the whole
-   * cache for every window row. */
   for (int w = 0; w < W; ++w) {
     double* row = P + (size_t)w * T;
     double m = -INFINITY;
@@ -109,43 +93,118 @@ int nxo_slice_scores(int T, int d, int W, int H, double lambda, double eps_tie,
     if (rowmax) rowmax[w] = m;
     if (rowsum) rowsum[w] = z;
   }
+}
 
+/*
+ * Eqs. (3), (4), (2), (5) over N scoring units (tokens at b = 1, blocks at
+ * b > 1), from the W per-row distributions P (W x N). Outputs as in
+ * nxo_slice_scores. Returns 0, or -1 on allocation failure.
+ */
+static int nxo_weights_from_rows(int N, int W, int H, double lambda, double eps_tie,
+                                 const double* P, double* a, double* ctilde, double* s,
+                                 float* w32, double* gamma) {
+  double* C = (double*)calloc((size_t)N, sizeof(double));
+  double* ab = (double*)malloc(sizeof(double) * (size_t)N);
+  double* cb = (double*)malloc(sizeof(double) * (size_t)N);
+  if (!C || !ab || !cb) {
+    free(C); free(ab); free(cb);
+    return -1;
+  }
   /* Eq. (3): the direct score is the uniform average of the W rows. */
-  for (int j = 0; j < T; ++j) {
+  for (int j = 0; j < N; ++j) {
     double acc = 0.0;
-    for (int w = 0; w < W; ++w) acc += P[(size_t)w * T + j];
+    for (int w = 0; w < W; ++w) acc += P[(size_t)w * N + j];
     ab[j] = acc / (double)W;
   }
 
   /* Eq. (4): C starts at 0; each of the last H rows, oldest first, is plugged
    * in once: gamma = 1 + <a^(q), C>, then C += gamma a^(q). */
   for (int t = 0; t < H; ++t) {
-    const double* row = P + (size_t)(W - H + t) * T;
+    const double* row = P + (size_t)(W - H + t) * N;
     double inner = 0.0;
-    for (int j = 0; j < T; ++j) inner += row[j] * C[j];
+    for (int j = 0; j < N; ++j) inner += row[j] * C[j];
     double g = 1.0 + inner;
     if (gamma) gamma[t] = g;
-    for (int j = 0; j < T; ++j) C[j] += g * row[j];
+    for (int j = 0; j < N; ++j) C[j] += g * row[j];
   }
   /* c~ = C / ||C||_1; an empty walk (H = 0) leaves c~ = 0. */
   double l1 = 0.0;
-  for (int j = 0; j < T; ++j) l1 += fabs(C[j]);
-  for (int j = 0; j < T; ++j) cb[j] = (H > 0 && l1 > 0.0) ? C[j] / l1 : 0.0;
+  for (int j = 0; j < N; ++j) l1 += fabs(C[j]);
+  for (int j = 0; j < N; ++j) cb[j] = (H > 0 && l1 > 0.0) ? C[j] / l1 : 0.0;
 
-  /* Eq. (2) and Eq. (5): s = a + lambda c~, w = s + eps_tie * j / (T - 1). */
-  for (int j = 0; j < T; ++j) {
+  /* Eq. (2) and Eq. (5): s = a + lambda c~, w = s + eps_tie * j / (N - 1). */
+  for (int j = 0; j < N; ++j) {
     double sj = ab[j] + lambda * cb[j];
-    double r = (T > 1) ? (double)j / (double)(T - 1) : 0.0;
+    double r = (N > 1) ? (double)j / (double)(N - 1) : 0.0;
     double wj = sj + eps_tie * r;
     if (a) a[j] = ab[j];
     if (ctilde) ctilde[j] = cb[j];
     if (s) s[j] = sj;
     if (w32) w32[j] = (float)wj;
   }
-
-  if (!P_out) free(P);
   free(C); free(ab); free(cb);
   return 0;
+}
+
+/*
+ * K: T x d rows of cached keys; Qbar: W x d window queries (already averaged
+ * over the query heads of the group). All outputs are optional (NULL skips);
+ * P (W x T) is the per-row distribution a^(q) of Eq. (3). Block size b = 1:
+ * BlockSum and rownorm of Eq. (1) are identities.
+ *
+ * Returns 0 on success, -1 on bad sizes or allocation failure.
+ */
+int nxo_slice_scores(int T, int d, int W, int H, double lambda, double eps_tie,
+                     const double* K, const double* Qbar, double* P_out,
+                     double* a, double* ctilde, double* s, float* w32,
+                     double* rowmax, double* rowsum, double* gamma) {
+  if (T < 1 || d < 1 || W < 1 || H < 0 || H > W) return -1;
+  double* P = P_out ? P_out : (double*)malloc(sizeof(double) * (size_t)W * T);
+  if (!P) return -1;
+  nxo_softmax_rows(T, d, W, K, Qbar, P, rowmax, rowsum);
+  int rc = nxo_weights_from_rows(T, W, H, lambda, eps_tie, P, a, ctilde, s, w32, gamma);
+  if (!P_out) free(P);
+  return rc;
+}
+
+/*
+ * Eq. (1) at block size b > 1 (§2.1 "Block granularity"): the token softmax rows
+ * are summed over blocks of b consecutive slots (BlockSum_b; the last block
+ * holds the T mod b remaining slots when b does not divide T) and each row is
+ * renormalised to sum 1 (rownorm), giving W rows over N_k = ceil(T / b) blocks;
+ * then Eqs. (3), (4), (2), (5) run over blocks, the tie-break ramp over the
+ * block index j / (N_k - 1). Outputs have N_k entries; Pb_out (optional) is the
+ * W x N_k block distribution. Returns N_k, or -1 on bad sizes / allocation.
+ */
+int nxo_block_scores(int T, int d, int W, int H, int b, double lambda, double eps_tie,
+                     const double* K, const double* Qbar, double* Pb_out, double* a,
+                     double* ctilde, double* s, float* w32, double* gamma) {
+  if (T < 1 || d < 1 || W < 1 || H < 0 || H > W || b < 1) return -1;
+  const int N = (T + b - 1) / b;
+  double* P = (double*)malloc(sizeof(double) * (size_t)W * T);
+  double* Pb = Pb_out ? Pb_out : (double*)malloc(sizeof(double) * (size_t)W * N);
+  if (!P || !Pb) {
+    free(P);
+    if (!Pb_out) free(Pb);
+    return -1;
+  }
+  nxo_softmax_rows(T, d, W, K, Qbar, P, NULL, NULL);
+  for (int w = 0; w < W; ++w) {
+    const double* row = P + (size_t)w * T;
+    double* brow = Pb + (size_t)w * N;
+    double tot = 0.0;
+    for (int B = 0; B < N; ++B) {
+      double acc = 0.0;
+      for (int j = B * b; j < T && j < (B + 1) * b; ++j) acc += row[j];
+      brow[B] = acc;
+      tot += acc;
+    }
+    for (int B = 0; B < N; ++B) brow[B] /= tot;   /* rownorm */
+  }
+  int rc = nxo_weights_from_rows(N, W, H, lambda, eps_tie, Pb, a, ctilde, s, w32, gamma);
+  free(P);
+  if (!Pb_out) free(Pb);
+  return rc == 0 ? N : -1;
 }
 
 /* ------------------------------------------------------------------------ */
@@ -242,6 +301,54 @@ void nxo_ln_spec_many(int64_t n, const float* u, float* out) {
   for (int64_t i = 0; i < n; ++i) out[i] = nxo_ln_spec(u[i]);
 }
 
+/* ------------------------------------------------------------------------ */
+/* exp_spec: a fully specified binary32 exponential                          */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Textbook method (Cody & Waite argument reduction, then the Taylor series):
+ *   k = round-to-nearest-even(x / ln 2) (x * (1/ln 2) rounded to binary32 first),
+ *   r = (x - k ln2_hi) - k ln2_lo   with ln 2 = ln2_hi + ln2_lo as in ln_spec
+ *                                   (16-bit ln2_hi, so k ln2_hi is exact),
+ *   e^r = 1 + r + r^2/2! + ... + r^7/7!  by Horner from the r^7/7! term,
+ *   e^x = e^r * 2^k.
+ * |r| <= ln(2)/2, so the truncated series is within 1e-8 relative. Results with
+ * k < -126 (below the smallest normal scale) are flushed to 0, k > 127 gives
+ * +inf. Every + and * is one binary32 rounding, in the fixed order below.
+ */
+float nxo_exp_spec(float x) {
+  const float inv_ln2 = 1.44269504088896340736f;
+  const float ln2_hi = 45426.0f / 65536.0f;
+  const float ln2_lo = (float)(0.69314718055994530942 - 45426.0 / 65536.0);
+  const float c2 = 1.0f / 2.0f, c3 = 1.0f / 6.0f, c4 = 1.0f / 24.0f, c5 = 1.0f / 120.0f;
+  const float c6 = 1.0f / 720.0f, c7 = 1.0f / 5040.0f;
+  if (x != x) return x;
+  float t = x * inv_ln2;
+  float kf = rintf(t);
+  if (kf < -126.0f) return 0.0f;
+  if (kf > 127.0f) return INFINITY;
+  float hi = kf * ln2_hi;
+  float lo = kf * ln2_lo;
+  float r = x - hi;
+  r = r - lo;
+  float p = c7;
+  p = p * r; p = p + c6;
+  p = p * r; p = p + c5;
+  p = p * r; p = p + c4;
+  p = p * r; p = p + c3;
+  p = p * r; p = p + c2;
+  p = p * r; p = p + 1.0f;
+  p = p * r; p = p + 1.0f;
+  uint32_t sbits = (uint32_t)((int)kf + 127) << 23;
+  float scale;
+  memcpy(&scale, &sbits, 4);
+  return p * scale;
+}
+
+void nxo_exp_spec_many(int64_t n, const float* x, float* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = nxo_exp_spec(x[i]);
+}
+
 void nxo_philox_many(int64_t n, const uint32_t* ctr4, const uint32_t* key2, uint32_t* out4) {
   for (int64_t i = 0; i < n; ++i) nxo_philox4x32_10(ctr4 + 4 * i, key2, out4 + 4 * i);
 }
@@ -288,14 +395,57 @@ float nxo_reservoir_key(float w, int32_t pos, uint64_t seed, uint32_t step, uint
 }
 
 /*
- * Retention set S_t of one slice. Writes the new length's worth of kept slots,
- * ascending, into keep_idx and returns that length (min(T, B)). kappa (length
- * T, optional) receives the key of every candidate slot (NaN for forced slots).
- * Returns -1 on invalid arguments.
+ * The n-averaged priority of Eq. (6), pi_j = (1/n) sum_i (u_j^(i))^(1/w_j), in the
+ * log domain (at token-sized weights u^(1/w) underflows even in double):
+ *   l_i = ln(u_i), M = max_i l_i, r = 1 / w (one IEEE division),
+ *   key = M r + ln( sum_i exp((l_i - M) r) )  =  ln(n pi_j).
+ * The constant -ln n is left out: it does not change the order. Draw i uses
+ * word i mod 4 of the Philox block with draw group g = i / 4 in bits 24..31 of
+ * counter word 3 (so draws 0..3 share one block, and draw 0 is the n = 1 draw).
+ * Every operation is one binary32 rounding in the order written (ln_spec,
+ * exp_spec; the sum runs i = 0 .. n - 1). A zero weight (r = +inf) gives -inf.
+ * n = 1 is the plain key ln(u)/w above. n is at most 1024 (256 draw groups).
+ */
+float nxo_reservoir_key_n(float w, int32_t pos, uint64_t seed, uint32_t step, uint32_t head_id,
+                          uint32_t seq_id, int n) {
+  if (n <= 1) return nxo_reservoir_key(w, pos, seed, step, head_id, seq_id);
+  if (n > 1024) return NAN;
+  float l[1024];
+  uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+  uint32_t out[4] = {0, 0, 0, 0};
+  float M = -INFINITY;
+  for (int i = 0; i < n; ++i) {
+    if (i % 4 == 0) {
+      uint32_t g = (uint32_t)(i / 4);
+      uint32_t ctr[4] = {(uint32_t)pos, step, head_id, (seq_id & 0x00FFFFFFu) | (g << 24)};
+      nxo_philox4x32_10(ctr, key, out);
+    }
+    l[i] = nxo_ln_spec(nxo_uniform(out[i % 4]));
+    if (l[i] > M) M = l[i];
+  }
+  float r = 1.0f / w;
+  if (!(r < INFINITY)) return -INFINITY;
+  float S = 0.0f;
+  for (int i = 0; i < n; ++i) {
+    float dlt = l[i] - M;
+    float x = dlt * r;
+    S = S + nxo_exp_spec(x);
+  }
+  float head = M * r;
+  return head + nxo_ln_spec(S);
+}
+
+/*
+ * Retention set S_t of one slice over T decision units (slots at b = 1, blocks
+ * at b > 1; pos is each unit's absolute position, a block's being that of its
+ * first token). Writes the min(T, B) kept units, ascending, into keep_idx and
+ * returns that count. kappa (length T, optional) receives the key of every
+ * candidate unit (NaN for forced units). n_avg is the averaging count n of
+ * Eq. (6) (1: Efraimidis-Spirakis keys). Returns -1 on invalid arguments.
  */
 int nxo_select_slice(int T, const float* w32, const int32_t* pos, int B, int n_sink, int n_recent,
                      int mode, uint64_t seed, uint32_t step, uint32_t head_id, uint32_t seq_id,
-                     int32_t* keep_idx, float* kappa) {
+                     int n_avg, int32_t* keep_idx, float* kappa) {
   if (T < 0 || B < 0 || n_sink < 0 || n_recent < 0 || n_sink + n_recent > B) return -1;
   if (T <= B) {
     for (int j = 0; j < T; ++j) keep_idx[j] = j;
@@ -315,8 +465,9 @@ int nxo_select_slice(int T, const float* w32, const int32_t* pos, int B, int n_s
       if (kappa) kappa[j] = NAN;
       continue;
     }
-    float key = (mode == NXO_TOPK) ? w32[j]
-                                   : nxo_reservoir_key(w32[j], pos[j], seed, step, head_id, seq_id);
+    float key = (mode == NXO_TOPK)
+                    ? w32[j]
+                    : nxo_reservoir_key_n(w32[j], pos[j], seed, step, head_id, seq_id, n_avg);
     if (kappa) kappa[j] = key;
     cand[c].key = key;
     cand[c].slot = j;
@@ -350,10 +501,13 @@ typedef struct {
 typedef struct {
   int32_t window, walk_len, n_sink, n_recent, mode;
   double lambda, eps_tie;
-  const int32_t* budget;     /* [S] */
+  const int32_t* budget;     /* [S]: units kept per slice of sequence s */
   uint64_t seed;
   uint32_t step;
   int32_t seq_id_base, layer_id_base;
+  int32_t n_avg;             /* averaging count n of Eq. (6) (1: plain ES keys) */
+  int32_t block_size;        /* b: tokens per decision unit (1 or more) */
+  const int32_t* slice_budget; /* optional [L*S*Hkv]: overrides budget[s] per slice */
 } nxo_params;
 
 /* Row index (in units of rows) of slot j of slice (l, s, h). */
@@ -366,21 +520,26 @@ static int64_t nxo_row(const nxo_cache* c, int l, int s, int h, int j) {
 
 /*
  * One eviction step for the listed slices (slice id = (l * S + s) * Hkv + h;
- * sel == NULL means every slice). For slice number i of the list:
- *   keep_out[i * cap ...]  the kept slots (first new_len entries),
- *   w_out[i * cap ...]     the binary32 weight w of every slot j < T,
- *   a_out[i * cap ...]     the direct score a (double),
- *   newlen_out[i]          min(T, B).
+ * sel == NULL means every slice). Decisions are made per unit of b = block_size
+ * consecutive slots (b = 1: per token; the last block of a slice holds the
+ * T mod b remaining slots when b does not divide T); the budget B, n_sink and
+ * n_recent count units. For slice number i of the list:
+ *   keep_out[i * cap ...]  the kept units, ascending (first min(N, B) entries,
+ *                          N = ceil(T / b) units),
+ *   w_out[i * cap ...]     the binary32 weight w of every unit,
+ *   a_out[i * cap ...]     the direct score a (double) of every unit,
+ *   newlen_out[i]          the rows left: the total size of the kept units.
  * Any of the outputs may be NULL. With mutate != 0 the K, V and pos rows of the
- * listed slices are compacted in place (row i <- row keep[i]) and lens updated.
+ * listed slices are compacted in place (the kept units' rows, in order, become
+ * slots 0 .. newlen - 1) and lens updated.
  * Returns 0, or -1 on an invalid argument or allocation failure.
  */
 int nxo_evict_step(nxo_cache* c, const void* q, const nxo_params* p, int n_sel,
                    const int32_t* sel, int32_t* keep_out, float* w_out, double* a_out,
                    int32_t* newlen_out, int mutate, int nthreads) {
   const int L = c->layers, S = c->seqs, Hk = c->kv_heads, G = c->group, d = c->head_dim;
-  const int W = p->window, H = p->walk_len, cap = c->capacity;
-  if (H > W || H < 0 || W < 1 || G < 1 || d < 1) return -1;
+  const int W = p->window, H = p->walk_len, cap = c->capacity, bs = p->block_size;
+  if (H > W || H < 0 || W < 1 || G < 1 || d < 1 || bs < 1) return -1;
   int n = sel ? n_sel : L * S * Hk;
   int failed = 0;
 #ifdef _OPENMP
@@ -391,7 +550,8 @@ int nxo_evict_step(nxo_cache* c, const void* q, const nxo_params* p, int n_sel,
     int sid = sel ? sel[i] : i;
     int h = sid % Hk, s = (sid / Hk) % S, l = sid / (Hk * S);
     int T = c->lens[sid];
-    int B = p->budget[s];
+    int B = p->slice_budget ? p->slice_budget[sid] : p->budget[s];
+    int N = (T + bs - 1) / bs;                     /* decision units */
     double* K = (double*)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1) * d);
     double* Qb = (double*)calloc((size_t)W * d, sizeof(double));
     double* a = (double*)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
@@ -404,8 +564,9 @@ int nxo_evict_step(nxo_cache* c, const void* q, const nxo_params* p, int n_sel,
       for (int j = 0; j < T; ++j) {
         int64_t r = nxo_row(c, l, s, h, j);
         for (int k = 0; k < d; ++k) K[(size_t)j * d + k] = nxo_load(c->k, c->dtype, r * d + k);
-        pj[j] = c->pos[r];
       }
+      /* a unit's position is that of its first slot */
+      for (int u = 0; u < N; ++u) pj[u] = c->pos[nxo_row(c, l, s, h, u * bs)];
       /* The window query of the KV group: mean of its G query heads. */
       for (int w_ = 0; w_ < W; ++w_)
         for (int k = 0; k < d; ++k) {
@@ -417,24 +578,35 @@ int nxo_evict_step(nxo_cache* c, const void* q, const nxo_params* p, int n_sel,
           }
           Qb[(size_t)w_ * d + k] = acc / (double)G;
         }
-      int rc = 0, nl = 0;
-      if (T > 0)
-        rc = nxo_slice_scores(T, d, W, H, p->lambda, p->eps_tie, K, Qb, NULL, a, NULL, NULL, w,
-                              NULL, NULL, NULL);
+      int rc = 0, nk = 0;
+      if (T > 0) {
+        if (bs == 1)
+          rc = nxo_slice_scores(T, d, W, H, p->lambda, p->eps_tie, K, Qb, NULL, a, NULL, NULL, w,
+                                NULL, NULL, NULL);
+        else
+          rc = nxo_block_scores(T, d, W, H, bs, p->lambda, p->eps_tie, K, Qb, NULL, a, NULL,
+                                NULL, w, NULL) == N ? 0 : -1;
+      }
       if (rc == 0) {
         uint32_t head_id = (uint32_t)((p->layer_id_base + l) * Hk + h);
         uint32_t seq_id = (uint32_t)(p->seq_id_base + s);
-        nl = nxo_select_slice(T, w, pj, B, p->n_sink, p->n_recent, p->mode, p->seed, p->step,
-                              head_id, seq_id, keep, NULL);
+        nk = nxo_select_slice(N, w, pj, B, p->n_sink, p->n_recent, p->mode, p->seed, p->step,
+                              head_id, seq_id, p->n_avg, keep, NULL);
       }
-      if (rc != 0 || nl < 0) {
+      if (rc != 0 || nk < 0) {
         failed |= 1;
       } else {
-        if (keep_out) {
-          for (int j = 0; j < nl; ++j) keep_out[(size_t)i * cap + j] = keep[j];
+        /* rows kept: whole units, the last (partial) unit with its own size */
+        int nl = 0;
+        for (int u = 0; u < nk; ++u) {
+          int size = T - keep[u] * bs;
+          nl += size < bs ? size : bs;
         }
-        if (w_out) for (int j = 0; j < T; ++j) w_out[(size_t)i * cap + j] = w[j];
-        if (a_out) for (int j = 0; j < T; ++j) a_out[(size_t)i * cap + j] = a[j];
+        if (keep_out) {
+          for (int u = 0; u < nk; ++u) keep_out[(size_t)i * cap + u] = keep[u];
+        }
+        if (w_out) for (int u = 0; u < N; ++u) w_out[(size_t)i * cap + u] = w[u];
+        if (a_out) for (int u = 0; u < N; ++u) a_out[(size_t)i * cap + u] = a[u];
         if (newlen_out) newlen_out[i] = nl;
         if (mutate && nl < T) {
           /* §2.1: inference continues with K_S, V_S -- copy out, then back. */
@@ -446,12 +618,14 @@ int nxo_evict_step(nxo_cache* c, const void* q, const nxo_params* p, int n_sel,
           if (!kt || !vt || !pt) {
             failed |= 1;
           } else {
-            for (int j = 0; j < nl; ++j) {
-              int64_t r = nxo_row(c, l, s, h, keep[j]);
-              memcpy(kt + rb * j, (unsigned char*)c->k + rb * r, rb);
-              memcpy(vt + rb * j, (unsigned char*)c->v + rb * r, rb);
-              pt[j] = c->pos[r];
-            }
+            int o = 0;
+            for (int u = 0; u < nk; ++u)
+              for (int j = keep[u] * bs; j < T && j < (keep[u] + 1) * bs; ++j, ++o) {
+                int64_t r = nxo_row(c, l, s, h, j);
+                memcpy(kt + rb * o, (unsigned char*)c->k + rb * r, rb);
+                memcpy(vt + rb * o, (unsigned char*)c->v + rb * r, rb);
+                pt[o] = c->pos[r];
+              }
             for (int j = 0; j < nl; ++j) {
               int64_t r = nxo_row(c, l, s, h, j);
               memcpy((unsigned char*)c->k + rb * r, kt + rb * j, rb);
