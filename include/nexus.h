@@ -5,16 +5,21 @@
  * "Forget Without Compromise: Nexus Sampling for Streaming KV-Cache Eviction Under
  * Fixed Budgets": direct scores (§2.1 Eq. (1), §2.2 Eq. (3)), the Nexus walk and
  * weight (§2.2 Eqs. (2), (4), (5)), weighted reservoir selection of B survivors
- * (§2.3 Eq. (6) with n = 1, i.e. Efraimidis-Spirakis keys ln(u)/w), and the
- * in-place compaction that lets inference continue with K_S, V_S (§2.1,
- * "streaming view").
+ * (§2.3 Eq. (6): Efraimidis-Spirakis keys ln(u)/w at n = 1, the n-averaged
+ * priority for n > 1), and the in-place compaction that lets inference continue
+ * with K_S, V_S (§2.1, "streaming view"). Decisions are made per token (b = 1) or
+ * per block of 32 consecutive slots (§2.1 "Block granularity", b = 32).
  *
  * Terms
  *   slice   one (layer l, sequence s, KV head h); slices are independent.
  *           slice id = (l * seqs + s) * kv_heads + h.
  *   row     one cached (key, value) of one slice; slot j = its index 0..T-1.
  *   T       rows currently cached in a slice (lens[slice]).
- *   B       the budget: rows kept per slice of sequence s (budget[s]).
+ *   unit    what one keep/evict decision covers: a row (block_size b = 1) or a block
+ *           of b consecutive slots [u b, (u + 1) b) (the slice's last block holds the
+ *           T mod b remaining rows when b does not divide T); N = ceil(T / b) units.
+ *   B       the budget: units kept per slice of sequence s (budget[s], or
+ *           slice_budget[slice] when given).
  *   W, H    window rows and walk length; G = query heads per KV head.
  *
  * Conventions (every entry point)
@@ -27,7 +32,7 @@
  *     and reads after synchronising): NX_DEV_* bits below.
  *   - Calls on different streams are independent when their workspaces and
  *     outputs are disjoint. Two calls must not share a workspace concurrently.
- *   - Block granularity is b = 1 (one decision per token).
+ *   - Block granularity is b = 1 (one decision per token) or b = 32 (block_size).
  */
 #ifndef NEXUS_H_
 #define NEXUS_H_
@@ -45,7 +50,7 @@ typedef struct CUstream_st* nx_stream_t;
 typedef enum nx_status {
   NX_OK = 0,
   NX_ERR_INVALID_ARG = 1,   /* a size, pointer, alignment or parameter is out of range */
-  NX_ERR_UNSUPPORTED = 2,   /* valid for the method, not built here (n_avg > 1)        */
+  NX_ERR_UNSUPPORTED = 2,   /* valid for the method, not built here (block size not 1/32)*/
   NX_ERR_CUDA = 3,          /* a CUDA launch or memset failed                           */
   NX_ERR_TIMEOUT = 4,       /* reserved: device waits report through dev_status         */
   NX_ERR_WORKSPACE = 5,     /* ws is NULL, misaligned or smaller than required          */
@@ -58,7 +63,8 @@ enum {
                                the affected call are incomplete (the cache may be
                                partially compacted) */
   NX_DEV_BAD_LEN = 2,       /* lens[slice] < 0 or > capacity: slice left untouched */
-  NX_DEV_BAD_BUDGET = 4,    /* budget[s] < n_sink + n_recent or > budget_max: untouched */
+  NX_DEV_BAD_BUDGET = 4,    /* the slice's budget < n_sink + n_recent or > budget_max:
+                               slice left untouched */
   NX_DEV_BAD_PAGE = 8       /* a block_table entry is outside [0, num_pages): untouched */
 };
 
@@ -95,25 +101,44 @@ typedef struct nx_cache {
 
 /*
  * Step parameters. Defaults from the paper's implementation details (§5.1):
- * lambda = 0.5, eps_tie = 1e-6; the paper's W = 16, H = 3. n_sink / n_recent are the
- * forced attention-sink and recency slots of §2.3 (counted inside B; 32 each is the
- * default reading, one paper block each).
+ * lambda = 0.5, eps_tie = 1e-6, n = 5, b = 32; the paper's W = 16, H = 3. n_sink /
+ * n_recent are the forced attention-sink and recency units of §2.3 (counted inside B;
+ * at b = 1, 32 each is the default reading, one paper block each; at b = 32, one
+ * block each).
+ *
+ * Reservoir keys (§2.3 Eq. (6)), per candidate unit j with weight w_j, from Philox4x32-10
+ * with counter (pos_j, step, head id, seq id | g << 24) and key = seed, where pos_j is
+ * the absolute position of the unit's first row and g the draw group:
+ *   n_avg = 1: u = uniform(word 0 of group 0), key = ln(u) / w_j;
+ *   n_avg = n > 1: u_i = uniform(word i mod 4 of group i / 4), l_i = ln(u_i),
+ *     M = max_i l_i, r = 1 / w_j, key = M r + ln(sum_i exp((l_i - M) r)) = ln(n pi_j)
+ *     (the order of pi_j = (1/n) sum_i u_i^(1/w_j); -ln n is left out as it does not
+ *     change the order); a zero weight gives -inf.
+ * uniform(x) = (2 (x >> 9) + 1) 2^-24; ln and exp are the library's specified binary32
+ * functions (argument reduction by the exponent / Cody-Waite, then the atanh series
+ * through f^13 / the Taylor series through r^7, each operation one IEEE rounding), so
+ * the keys are reproducible bit for bit.
  */
 typedef struct nx_params {
   int32_t window;              /* W, 1..64 */
   int32_t walk_len;            /* H, 0..min(W, 8): the last H window rows, oldest first */
-  int32_t n_sink;              /* first n_sink slots always kept */
-  int32_t n_recent;            /* last n_recent slots always kept */
-  int32_t n_avg;               /* reservoir averaging count n of Eq. (6); must be 1 */
+  int32_t n_sink;              /* first n_sink units always kept */
+  int32_t n_recent;            /* last n_recent units always kept (>= 1 when b > 1) */
+  int32_t n_avg;               /* reservoir averaging count n of Eq. (6), 1..1024 */
   int32_t mode;                /* NX_MODE_RESERVOIR, or NX_MODE_TOPK (keep the top by w) */
   float lambda;                /* mixing weight of Eq. (2), >= 0 */
   float eps_tie;               /* recency tie-break of Eq. (5), >= 0 */
-  const int32_t* budget;       /* device int32 [seqs]: B per sequence */
-  int32_t budget_max;          /* host bound: every budget[s] <= budget_max <= capacity */
+  const int32_t* budget;       /* device int32 [seqs]: B (units) per sequence */
+  int32_t budget_max;          /* host bound: every budget <= budget_max <= ceil(capacity / b) */
   int32_t seq_id_base;         /* Philox sequence id of s is seq_id_base + s (< 2^24) */
   int32_t layer_id_base;       /* Philox head id of (l, h) is (layer_id_base + l) * kv_heads + h */
   uint32_t step;               /* Philox step id; callers advance it per eviction step */
   uint64_t seed;               /* Philox key */
+  int32_t block_size;          /* b: 1 (decisions per token) or 32 (per 32-slot block) */
+  int32_t reserved;            /* 0 */
+  const int32_t* slice_budget; /* nullable device int32 [slices]: a budget per slice (e.g.
+                                  from a head-adaptive allocation, §10); overrides
+                                  budget[s] for every slice when given */
 } nx_params;
 
 /*
@@ -123,12 +148,14 @@ typedef struct nx_params {
 size_t nexus_workspace_bytes(const nx_cache* cache, const nx_params* params);
 
 /*
- * Direct scores, §2.1 Eq. (1) at b = 1 and §2.2 Eq. (3):
+ * Direct scores, §2.1 Eq. (1) and §2.2 Eq. (3):
  *   Qbar_w = (1/G) sum_g q[g][w];  P_w = softmax_j(Qbar_w . k_j / sqrt(head_dim)) over
- *   the whole cache (no mask);     a_j = (1/W) sum_w P_w[j].
+ *   the whole cache (no mask);     a_j = (1/W) sum_w P_w[j]; at b > 1, P_w is summed
+ *   over each block (BlockSum; its rows still sum to 1, so rownorm is the identity)
+ *   and a has one entry per block.
  * q: [layers][seqs][kv_heads * group][window][head_dim] in cache->dtype (device,
  *    16-byte aligned); query head kv_head * group + g belongs to KV head kv_head.
- * a_out: float [slices][capacity], entries j < T written.
+ * a_out: float [slices][capacity], entries j < N (units) written.
  * row_stats_out (nullable): float [slices][window][2] = (max_j logit, sum_j exp(logit - max)).
  * Errors: NX_ERR_INVALID_ARG, NX_ERR_WORKSPACE, NX_ERR_CUDA. Empty slices (T = 0)
  * write nothing.
@@ -138,36 +165,41 @@ nx_status nexus_direct_scores(const nx_cache* cache, const void* q, const nx_par
                               int32_t* dev_status, nx_stream_t stream);
 
 /*
- * Nexus weight, §2.2 Eqs. (4), (2), (5):
+ * Nexus weight, §2.2 Eqs. (4), (2), (5), over the N units (rows, or blocks whose rows
+ * P_q are the block sums):
  *   C = 0; for the last H window rows q, oldest first: gamma_q = 1 + <P_q, C>,
  *   C += gamma_q P_q;  c~ = C / ||C||_1 (0 when H = 0);  s = a + lambda c~;
- *   w_j = s_j + eps_tie * j / (T - 1)  (the ramp is 0 when T = 1).
+ *   w_j = s_j + eps_tie * j / (N - 1)  (the ramp is 0 when N = 1).
  * Computes everything from the cache and q (same layout as nexus_direct_scores).
- * w_out: float [slices][capacity]; ctilde_out (nullable): float [slices][capacity].
+ * w_out: float [slices][capacity]; ctilde_out (nullable): float [slices][capacity];
+ * entries j < N written.
  */
 nx_status nexus_walk(const nx_cache* cache, const void* q, const nx_params* params, float* w_out,
                      float* ctilde_out, void* ws, size_t ws_bytes, int32_t* dev_status,
                      nx_stream_t stream);
 
 /*
- * Weighted reservoir selection, §2.3 and Eq. (6) with n = 1 (Efraimidis-Spirakis):
- *   forced F = slots [0, n_sink) and [T - n_recent, T); K = B - |F|;
- *   for j not in F: x = word 0 of Philox4x32-10(counter = (pos_j, step, head id,
- *   seq id), key = seed), u = (2 (x >> 9) + 1) 2^-24, kappa_j = ln(u) / w_j in
- *   binary32 (ln by the library's specified binary32 logarithm, IEEE division);
- *   keep the K largest (kappa desc, then slot desc) -- in NX_MODE_TOPK kappa_j = w_j.
- * w: float [slices][capacity] (device). keep_idx: int32 [slices][capacity]: the first
- * min(T, B) entries receive the kept slots in ascending order (0..T-1 when T <= B);
- * the rest are not written. The cache is read (lens, pos), not modified.
+ * Weighted reservoir selection, §2.3 and Eq. (6), over the N units of each slice:
+ *   forced F = units [0, n_sink) and [N - n_recent, N); K = B - |F|;
+ *   for j not in F: kappa_j = the reservoir key of nx_params (n_avg = 1: ln(u)/w_j,
+ *   Efraimidis-Spirakis; n_avg > 1: ln of the n-averaged priority); keep the K
+ *   largest (kappa desc, then unit desc) -- in NX_MODE_TOPK kappa_j = w_j.
+ * w: float [slices][capacity] (device), entries j < N. keep_idx: int32
+ * [slices][capacity]: the first min(N, B) entries receive the kept units in ascending
+ * order (0..N-1 when N <= B); the rest are not written. The cache is read (lens,
+ * pos), not modified.
  */
 nx_status nexus_reservoir_select(const float* w, const nx_cache* cache, const nx_params* params,
                                  int32_t* keep_idx, void* ws, size_t ws_bytes,
                                  int32_t* dev_status, nx_stream_t stream);
 
 /*
- * In-place compaction (§2.1: inference continues with K_S, V_S): for every slice with
- * n = min(T, B) and i < n, row i <- row keep_idx[i] (k, v and pos), then lens = n.
- * keep_idx: int32 [slices][capacity], ascending, as written by nexus_reservoir_select.
+ * In-place compaction (§2.1: inference continues with K_S, V_S): the rows of the kept
+ * units move, in order, to slots 0 .. n - 1 (k, v and pos), then lens = n. At b = 1,
+ * n = min(T, B) and row i <- row keep_idx[i]; at b > 1 row i <- row keep_idx[i / b] b +
+ * i mod b, and n = T when N <= B, else (B - 1) b + the size of the newest block (always
+ * kept: n_recent >= 1). keep_idx: int32 [slices][capacity], ascending kept units, as
+ * written by nexus_reservoir_select.
  * Rows at or beyond n and the block table are not modified; rows with
  * keep_idx[i] == i are not rewritten. Uses the workspace for tile flags; bounded
  * waits report NX_DEV_TIMEOUT.
@@ -186,7 +218,7 @@ nx_status kv_compact(nx_cache* cache, const int32_t* keep_idx, const nx_params* 
  * Its scratch (a tile counter, the new lengths, one flag per tile of kCompactRows = 32
  * rows) lives in a 4 MiB static device array inside libnexus.so, held by every GPU
  * that loads the library until the process exits. Limit: 256 + 4 * slices (rounded
- * up to 256) + 4 * slices * ceil(budget_max / 32) (rounded up to 256) bytes must fit
+ * up to 256) + 4 * slices * ceil(budget_max * b / 32) (rounded up to 256) bytes must fit
  * in 4 MiB; larger calls return NX_ERR_WORKSPACE without launching anything. The
  * function calls no cudaMalloc, cudaFree or other allocating routine.
  * Every call made outside a stream capture looks up the array's device address for the

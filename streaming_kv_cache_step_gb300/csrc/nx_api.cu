@@ -50,13 +50,19 @@ nx_status check_params(const nx_cache* c, const nx_params* p) {
   if (!(p->lambda >= 0.f) || !isfinite(p->lambda)) return NX_ERR_INVALID_ARG;
   if (!(p->eps_tie >= 0.f) || !isfinite(p->eps_tie)) return NX_ERR_INVALID_ARG;
   if (!p->budget) return NX_ERR_INVALID_ARG;
-  if (p->budget_max < p->n_sink + p->n_recent || p->budget_max > c->capacity)
+  if (p->block_size != 1 && p->block_size != 32) {
+    if (p->block_size < 1) return NX_ERR_INVALID_ARG;
+    return NX_ERR_UNSUPPORTED;
+  }
+  if (p->block_size > 1 && p->n_recent < 1) return NX_ERR_INVALID_ARG;   // newest block kept
+  if (p->reserved != 0) return NX_ERR_INVALID_ARG;
+  const int max_units = (c->capacity + p->block_size - 1) / p->block_size;
+  if (p->budget_max < p->n_sink + p->n_recent || p->budget_max > max_units)
     return NX_ERR_INVALID_ARG;
   if (p->seq_id_base < 0 || (long long)p->seq_id_base + c->seqs > (1LL << 24))
     return NX_ERR_INVALID_ARG;
   if (p->layer_id_base < 0) return NX_ERR_INVALID_ARG;
-  if (p->n_avg < 1) return NX_ERR_INVALID_ARG;
-  if (p->n_avg != 1) return NX_ERR_UNSUPPORTED;
+  if (p->n_avg < 1 || p->n_avg > kMaxAvg) return NX_ERR_INVALID_ARG;
   return NX_OK;
 }
 
@@ -65,7 +71,8 @@ WsLayout layout_of(const nx_cache* c, const nx_params* p) {
   L.slices = (long long)c->layers * c->seqs * c->kv_heads;
   L.max_chunks = (c->capacity + 127) / 128;
   L.stats_stride = (int)align_up(2 * p->window + kMaxPairs, 4);
-  L.tiles_per_slice = (p->budget_max + kCompactRows - 1) / kCompactRows;
+  L.tiles_per_slice =
+      (int)(((long long)p->budget_max * p->block_size + kCompactRows - 1) / kCompactRows);
   if (L.tiles_per_slice < 1) L.tiles_per_slice = 1;
   size_t o = 0;
   L.counters = o;
@@ -237,7 +244,7 @@ nx_status nexus_reservoir_select(const float* w_in, const nx_cache* cache, const
   uint32_t* keys = reinterpret_cast<uint32_t*>(w + L.keys);
   NX_TRY(launch_newlen(*cache, *params, newlen, dev_status, st, &launches));
   NX_TRY(launch_keys_from_w(*cache, *params, w_in, keys, newlen, st, &launches));
-  NX_TRY(launch_select(*cache, keys, keep_idx, newlen, st, &launches));
+  NX_TRY(launch_select(*cache, keys, keep_idx, newlen, params->block_size, st, &launches));
   return finish(cudaSuccess, launches);
 }
 
@@ -277,7 +284,7 @@ nx_status nexus_evict_step(nx_cache* cache, const void* q, const nx_params* para
   out.keys = keys;
   out.flags = kEmitKeys;
   NX_TRY(run_scores(*cache, q, *params, L, w, out, dev_status, st, &launches));
-  NX_TRY(launch_select(*cache, keys, keep, newlen, st, &launches));
+  NX_TRY(launch_select(*cache, keys, keep, newlen, params->block_size, st, &launches));
   NX_TRY(launch_compact(*cache, *params, L, w, keep, newlen, dev_status, st, &launches));
   return finish(cudaSuccess, launches);
 }

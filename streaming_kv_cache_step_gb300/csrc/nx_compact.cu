@@ -1,8 +1,10 @@
 // nx_compact.cu -- in-place stable compaction (Nexus Sampling paper, §2.1: inference
-// continues with K_S, V_S): row i <- row keep[i] for k, v and pos, i < n = min(T, B).
+// continues with K_S, V_S): row i <- row src(i) for k, v and pos, i < n, where src(i) =
+// keep[i] at block size b = 1 and keep[i / b] b + i mod b for blocks of b rows (keep holds
+// the kept units, ascending).
 //
-// keep is ascending with keep[i] >= i, so writing row i can only destroy a source that a
-// destination i' <= i still needs. Destinations are cut into tiles of kCompactRows rows,
+// keep is ascending with keep[u] >= u, so src(i) >= i and writing row i can only destroy a
+// source that a destination i' <= i still needs. Destinations are cut into tiles of kCompactRows rows,
 // claimed in increasing order through one global counter (which skips the empty tail
 // tiles of each slice). A tile first copies all its
 // sources into shared memory, then publishes "read done", then waits (bounded) until the
@@ -24,7 +26,7 @@ __device__ __forceinline__ bool slice_ok(const nx_cache& c, const nx_params& p, 
   int l, s, h;
   slice_coords(c, slice, l, s, h);
   const int T = c.lens[slice];
-  const int B = p.budget[s];
+  const int B = budget_of(p, slice, s);
   if (T < 0 || T > c.capacity) {
     atomicOr(dev_status, NX_DEV_BAD_LEN);
     return false;
@@ -57,7 +59,9 @@ __global__ void newlen_kernel(nx_cache c, nx_params p, int32_t* __restrict__ new
   if (slice >= slices) return;
   int l, s, h;
   slice_coords(c, (int)slice, l, s, h);
-  newlen[slice] = slice_ok(c, p, (int)slice, dev_status) ? min(c.lens[slice], p.budget[s]) : -1;
+  newlen[slice] = slice_ok(c, p, (int)slice, dev_status)
+                      ? rows_kept(c.lens[slice], budget_of(p, (int)slice, s), p.block_size)
+                      : -1;
 }
 
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
@@ -85,7 +89,7 @@ struct TileSlot {
 __global__ void __launch_bounds__(kCompactThreads)
 compact_kernel(nx_cache c, const int32_t* __restrict__ keep, const int32_t* __restrict__ newlen,
                int* tile_flags, unsigned long long* work, int tiles_per_slice,
-               long long total_tiles, int32_t* dev_status, long long skip_signal_tile) {
+               long long total_tiles, int32_t* dev_status, long long skip_signal_tile, int bs) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int row_bytes = c.head_dim * (c.dtype == NX_DTYPE_BF16 ? 2 : 4);
   const int chunks = row_bytes / 16;                    // 16-byte pieces per row
@@ -136,7 +140,10 @@ compact_kernel(nx_cache c, const int32_t* __restrict__ keep, const int32_t* __re
     bool mv = false;
     if (threadIdx.x < kCompactRows) {
       const int i = threadIdx.x;
-      const int src = (i < sl.n) ? kp[sl.i0 + i] : 0;
+      // source slot of destination slot i0 + i: the kept unit's row at the same offset
+      // (units are rows at b = 1, blocks of bs rows otherwise)
+      const int dst = sl.i0 + i;
+      const int src = (i < sl.n) ? (bs == 1 ? kp[dst] : kp[dst / bs] * bs + dst % bs) : 0;
       s_src[b][i] = src;
       mv = i < sl.n && src != sl.i0 + i;
       if (mv) {
@@ -223,7 +230,6 @@ cudaError_t launch_newlen(const nx_cache& c, const nx_params& p, int32_t* newlen
 cudaError_t launch_compact(const nx_cache& c, const nx_params& p, const WsLayout& L, char* ws,
                            const int32_t* keep, const int32_t* newlen, int32_t* dev_status,
                            cudaStream_t st, int* launches, long long skip_signal_tile) {
-  (void)p;
   const int row_bytes = c.head_dim * (c.dtype == NX_DTYPE_BF16 ? 2 : 4);
   const size_t smem = 2 * 2 * (size_t)kCompactRows * row_bytes;   // two buffers of K + V
   int dev = 0, sms = 0, per_sm = 0;
@@ -242,7 +248,7 @@ cudaError_t launch_compact(const nx_cache& c, const nx_params& p, const WsLayout
   const cudaError_t e = launch_after(
       compact_kernel, dim3((unsigned)grid), dim3(kCompactThreads), smem, st, c, keep, newlen,
       reinterpret_cast<int*>(ws + L.tile_flags), reinterpret_cast<unsigned long long*>(ws + L.work),
-      (int)L.tiles_per_slice, total, dev_status, skip_signal_tile);
+      (int)L.tiles_per_slice, total, dev_status, skip_signal_tile, p.block_size);
   if (e != cudaSuccess) return e;
   note_launch(st, launches, "compact");
   return cudaGetLastError();

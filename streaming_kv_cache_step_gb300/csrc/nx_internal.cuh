@@ -16,6 +16,8 @@ namespace nx {
 // ---------------------------------------------------------------------------
 constexpr int kMaxWindow = 64;        // W <= 64
 constexpr int kMaxWalk = 8;           // H <= 8
+constexpr int kMaxAvg = 1024;         // n_avg <= 1024 (256 Philox draw groups)
+constexpr int kBlockRows = 32;        // the block size b > 1 (one warp's rows)
 constexpr int kMaxPairs = kMaxWalk * (kMaxWalk - 1) / 2;   // walk-row pairs u < t
 constexpr int kSimtRows = 256;        // rows per thread block in the CUDA-core scorer
 constexpr int kCompactRows = 32;      // destination rows per compaction tile
@@ -145,15 +147,110 @@ __device__ __forceinline__ float ln_spec(float u) {
   return __fadd_rn(__fmul_rn(ef, kLn2Hi), __fadd_rn(__fmul_rn(ef, kLn2Lo), lnm));
 }
 
-// Order key of one candidate slot (§2.3, Eq. (6) with n = 1): ln(u)/w for the reservoir,
-// w itself for the top-K template.
+// Specified binary32 exponential (Cody & Waite): k = round-half-even(x * (1/ln 2)),
+// r = (x - k ln2_hi) - k ln2_lo with the 16-bit ln2_hi of ln_spec (k ln2_hi exact),
+// e^r by its Taylor series through r^7/7! (Horner from the top term), times 2^k; k < -126
+// flushes to 0, k > 127 gives +inf. One IEEE round-to-nearest operation per step, in a
+// fixed order, so any implementation of the same recipe gives the same bits.
+__device__ __forceinline__ float exp_spec(float x) {
+  constexpr float kInvLn2 = 1.44269504088896340736f;
+  constexpr float kLn2Hi = 45426.0f / 65536.0f;
+  constexpr float kLn2Lo = (float)(0.69314718055994530942 - 45426.0 / 65536.0);
+  constexpr float c2 = 1.0f / 2.0f, c3 = 1.0f / 6.0f, c4 = 1.0f / 24.0f;
+  constexpr float c5 = 1.0f / 120.0f, c6 = 1.0f / 720.0f, c7 = 1.0f / 5040.0f;
+  if (x != x) return x;
+  const float kf = rintf(__fmul_rn(x, kInvLn2));
+  if (kf < -126.0f) return 0.0f;
+  if (kf > 127.0f) return __int_as_float(0x7F800000);
+  float r = __fsub_rn(x, __fmul_rn(kf, kLn2Hi));
+  r = __fsub_rn(r, __fmul_rn(kf, kLn2Lo));
+  float h = c7;
+  h = __fadd_rn(__fmul_rn(h, r), c6);
+  h = __fadd_rn(__fmul_rn(h, r), c5);
+  h = __fadd_rn(__fmul_rn(h, r), c4);
+  h = __fadd_rn(__fmul_rn(h, r), c3);
+  h = __fadd_rn(__fmul_rn(h, r), c2);
+  h = __fadd_rn(__fmul_rn(h, r), 1.0f);
+  h = __fadd_rn(__fmul_rn(h, r), 1.0f);
+  return __fmul_rn(h, __uint_as_float((uint32_t)((int)kf + 127) << 23));
+}
+
+// The Philox block of draw group g of one candidate: counter (pos, step, head id,
+// seq id | g << 24), key = the 64-bit seed.
+__device__ __forceinline__ uint4 draw_block(int32_t pos, const nx_params& p, uint32_t head_id,
+                                            uint32_t seq_id, uint32_t g) {
+  return philox4x32_10(
+      make_uint4((uint32_t)pos, p.step, head_id, (seq_id & 0x00FFFFFFu) | (g << 24)),
+      (uint32_t)p.seed, (uint32_t)(p.seed >> 32));
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// ln of uniform i of a candidate (word i mod 4 of draw group i / 4)
+__device__ __forceinline__ float log_draw(int32_t pos, const nx_params& p, uint32_t head_id,
+                                          uint32_t seq_id, int i) {
+  return ln_spec(word_to_uniform(word_of(draw_block(pos, p, head_id, seq_id, (uint32_t)i >> 2),
+                                         i & 3)));
+}
+
+// §2.3 Eq. (6) for n > 1, in the log domain: with l_i = ln(u_i), M = max_i l_i and
+// r = 1/w, key = M r + ln(sum_{i < n} exp((l_i - M) r)) = ln(n pi_j); -inf for w = 0.
+// Up to 8 draws stay in registers; more are drawn twice (same values both times).
+static __device__ __noinline__ float averaged_key(float w, int32_t pos, const nx_params& p,
+                                           uint32_t head_id, uint32_t seq_id) {
+  const int n = p.n_avg;
+  float l8[8];
+  float M = -__int_as_float(0x7F800000);
+  uint4 blk = make_uint4(0, 0, 0, 0);
+  for (int i = 0; i < n; ++i) {
+    if ((i & 3) == 0) blk = draw_block(pos, p, head_id, seq_id, (uint32_t)i >> 2);
+    const float l = ln_spec(word_to_uniform(word_of(blk, i & 3)));
+    if (i < 8) l8[i] = l;
+    M = fmaxf(M, l);
+  }
+  const float r = __fdiv_rn(1.0f, w);
+  if (!(r < __int_as_float(0x7F800000))) return -__int_as_float(0x7F800000);
+  float S = 0.0f;
+  for (int i = 0; i < n; ++i) {
+    float l;
+    if (n <= 8) {
+      l = l8[i];
+    } else {
+      if ((i & 3) == 0) blk = draw_block(pos, p, head_id, seq_id, (uint32_t)i >> 2);
+      l = ln_spec(word_to_uniform(word_of(blk, i & 3)));
+    }
+    S = __fadd_rn(S, exp_spec(__fmul_rn(__fsub_rn(l, M), r)));
+  }
+  return __fadd_rn(__fmul_rn(M, r), ln_spec(S));
+}
+
+// Order key of one candidate unit (§2.3, Eq. (6)): ln(u)/w for the reservoir at n = 1
+// (Efraimidis-Spirakis), the log of the n-averaged priority for n > 1, w itself for the
+// top-K template.
 __device__ __forceinline__ uint32_t candidate_key(float w, int32_t pos, const nx_params& p,
                                                   uint32_t head_id, uint32_t seq_id) {
   if (p.mode == NX_MODE_TOPK) return order_key(w);
-  const uint4 r = philox4x32_10(make_uint4((uint32_t)pos, p.step, head_id, seq_id & 0x00FFFFFFu),
-                                (uint32_t)p.seed, (uint32_t)(p.seed >> 32));
+  if (p.n_avg > 1) return order_key(averaged_key(w, pos, p, head_id, seq_id));
+  const uint4 r = draw_block(pos, p, head_id, seq_id, 0);
   return order_key(__fdiv_rn(ln_spec(word_to_uniform(r.x)), w));
 }
+
+// The budget (units kept) of a slice: its own when the caller gives per-slice budgets.
+__device__ __forceinline__ int budget_of(const nx_params& p, int slice, int s) {
+  return p.slice_budget ? p.slice_budget[slice] : p.budget[s];
+}
+
+// Rows left in a slice of T rows after keeping B units of b rows (B >= 1): every kept
+// unit is whole except the newest block, which is always kept (n_recent >= 1 at b > 1).
+__host__ __device__ __forceinline__ int rows_kept(int T, int B, int b) {
+  const int N = (T + b - 1) / b;
+  return N <= B ? T : (B - 1) * b + (T - (N - 1) * b);
+}
+
+// Units of a slice of T rows.
+__host__ __device__ __forceinline__ int units_of(int T, int b) { return (T + b - 1) / b; }
 
 __device__ __forceinline__ int ld_acquire(const int* addr) {
   int v;
@@ -246,7 +343,8 @@ cudaError_t launch_keys_from_w(const nx_cache& c, const nx_params& p, const floa
                                uint32_t* keys, const int32_t* newlen, cudaStream_t st,
                                int* launches);
 cudaError_t launch_select(const nx_cache& c, const uint32_t* keys, int32_t* keep,
-                          const int32_t* newlen, cudaStream_t st, int* launches);
+                          const int32_t* newlen, int block_size, cudaStream_t st,
+                          int* launches);
 // nx_compact.cu
 cudaError_t launch_newlen(const nx_cache& c, const nx_params& p, int32_t* newlen,
                           int32_t* dev_status, cudaStream_t st, int* launches);

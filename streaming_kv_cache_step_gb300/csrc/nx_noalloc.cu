@@ -58,7 +58,8 @@ extern "C" nx_status kv_compact_noalloc(nx_cache* cache, const int32_t* keep_idx
   begin_call();
   // Same argument checks as the workspace-taking entry points (0 = rejected).
   if (nexus_workspace_bytes(cache, params) == 0) {
-    if (params && cache && params->n_avg > 1) return NX_ERR_UNSUPPORTED;
+    if (params && cache && params->block_size > 1 && params->block_size != 32)
+      return NX_ERR_UNSUPPORTED;
     return NX_ERR_INVALID_ARG;
   }
   if (!keep_idx || !dev_status) return NX_ERR_INVALID_ARG;
@@ -66,7 +67,8 @@ extern "C" nx_status kv_compact_noalloc(nx_cache* cache, const int32_t* keep_idx
   // Scratch layout inside the static array: claim counter | new lengths | tile flags.
   WsLayout L{};
   L.slices = (long long)cache->layers * cache->seqs * cache->kv_heads;
-  L.tiles_per_slice = (params->budget_max + kCompactRows - 1) / kCompactRows;
+  L.tiles_per_slice = (int)(((long long)params->budget_max * params->block_size +
+                             kCompactRows - 1) / kCompactRows);
   if (L.tiles_per_slice < 1) L.tiles_per_slice = 1;
   L.work = 0;
   L.newlen = 256;

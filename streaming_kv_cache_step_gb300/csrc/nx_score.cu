@@ -55,7 +55,7 @@ __global__ void prep_kernel(nx_cache c, const void* __restrict__ q, nx_params p,
     __shared__ int bad;
     if (threadIdx.x == 0) {
       bad = 0;
-      const int B = p.budget[s];
+      const int B = budget_of(p, slice, s);
       if (T < 0 || T > c.capacity) {
         atomicOr(dev_status, NX_DEV_BAD_LEN);
         bad = 1;
@@ -77,7 +77,8 @@ __global__ void prep_kernel(nx_cache c, const void* __restrict__ q, nx_params p,
       }
     }
     __syncthreads();
-    if (threadIdx.x == 0) newlen[slice] = bad ? -1 : min(T, p.budget[s]);
+    if (threadIdx.x == 0)
+      newlen[slice] = bad ? -1 : rows_kept(T, budget_of(p, slice, s), p.block_size);
   }
   if (mode == 0) return;
   const int n = blockIdx.y;                        // window row
@@ -231,6 +232,18 @@ score_simt_kernel(nx_cache c, nx_params p, const float* __restrict__ qbar,
         if (t < H && w == W - H + t) x = e[w];
       ew[t] = x;
     }
+    if (p.block_size > 1) {
+      // b = 32: the walk takes inner products between block rows (sums over the 32 rows
+      // of a block, which are this warp's rows); lane 0 carries the block's terms
+      const int lane = threadIdx.x & 31;
+#pragma unroll
+      for (int t = 0; t < kMaxWalk; ++t) {
+        float x = ew[t];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+        ew[t] = lane == 0 ? x : 0.f;
+      }
+    }
     float gc[kMaxPairs];
 #pragma unroll
     for (int t = 0; t < kMaxWalk; ++t)
@@ -297,26 +310,40 @@ score_simt_kernel(nx_cache c, nx_params p, const float* __restrict__ qbar,
       out.row_stats[((long long)slice * W + w) * 2 + 1] = ssum[w];
     }
   }
-  if (!valid) return;
+  const int bs = p.block_size;
+  if (bs == 1 && !valid) return;
   float a = 0.f, ct = 0.f;
 #pragma unroll
   for (int w = 0; w < WMAX; ++w) {
     if (w < W) {
-      const float e = expf(lg[w] - smax[w]);
+      const float e = valid ? expf(lg[w] - smax[w]) : 0.f;
       a = fmaf(e, scoef[w], a);
       if (w >= W - H) ct = fmaf(e, swalk[w - (W - H)], ct);
     }
   }
+  int u = j;                      // the decision unit: this row, or its 32-row block
+  if (bs > 1) {
+    // Eq. (1) BlockSum: a block's scores are the sums over its rows (this warp's 32
+    // rows, blocks being aligned to warps); lane 0 finalizes the block
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      a += __shfl_xor_sync(0xffffffffu, a, o);
+      ct += __shfl_xor_sync(0xffffffffu, ct, o);
+    }
+    if ((threadIdx.x & 31) != 0 || !valid) return;
+    u = j / bs;
+  }
+  const int N = units_of(T, bs);
   const float sj = a + p.lambda * ct;
-  const float ramp = (T > 1) ? (float)j / (float)(T - 1) : 0.f;
+  const float ramp = (N > 1) ? (float)u / (float)(N - 1) : 0.f;
   const float wj = sj + p.eps_tie * ramp;
-  const long long o = (long long)slice * c.capacity + j;
+  const long long o = (long long)slice * c.capacity + u;
   if (out.flags & kEmitA) out.a[o] = a;
   if (out.flags & kEmitC) out.ctilde[o] = ct;
   if (out.flags & kEmitW) out.w[o] = wj;
   if (out.flags & kEmitKeys) {
     uint32_t key = kForcedKey;
-    if (!(j < p.n_sink || j >= T - p.n_recent)) {
+    if (!(u < p.n_sink || u >= N - p.n_recent)) {
       const uint32_t head_id = (uint32_t)((p.layer_id_base + l) * c.kv_heads + h);
       key = candidate_key(wj, c.pos[r], p, head_id, (uint32_t)(p.seq_id_base + s));
     }

@@ -543,6 +543,7 @@ struct Epi {
   template <int HT>
   __device__ void stats(const Chunk& ch) {
     constexpr int RS = Smem<W, D, NWG>::kRedStride;
+    const bool blocks = A.p.block_size > 1;
     float* m = mc(ch.b);
     float mx[CW];
 #pragma unroll
@@ -610,13 +611,10 @@ struct Epi {
         tmem_stn<CW>(taddr(ch, t), v);
         if (walk_wg) {
           float ew[kMaxWalk];
+          constexpr int NW = HT >= 0 ? HT : kMaxWalk;     // walk columns carried
           if (HT >= 0) {
 #pragma unroll
             for (int tt = 0; tt < kMaxWalk; ++tt) ew[tt] = (tt < HT) ? v[CW - HT + tt] : 0.f;
-#pragma unroll
-            for (int tt = 1; tt < (HT > 0 ? HT : 1); ++tt)
-#pragma unroll
-              for (int uu = 0; uu < tt; ++uu) gp[pair_index(uu, tt)] += ew[uu] * ew[tt];
           } else {
 #pragma unroll
             for (int tt = 0; tt < kMaxWalk; ++tt) {
@@ -626,11 +624,21 @@ struct Epi {
                 if (tt < H && i == CW - H + tt) x = v[i];
               ew[tt] = x;
             }
-#pragma unroll
-            for (int tt = 1; tt < kMaxWalk; ++tt)
-#pragma unroll
-              for (int uu = 0; uu < tt; ++uu) gp[pair_index(uu, tt)] += ew[uu] * ew[tt];
           }
+          if (blocks) {
+            // b = 32: the walk's inner products are between block rows, the sums over the
+            // 32 rows of a block -- this warp's rows (chunks start at multiples of 128);
+            // lane 0 carries the block's products
+#pragma unroll
+            for (int tt = 0; tt < NW; ++tt) {
+              const float x = warp_sum(ew[tt]);
+              ew[tt] = lane == 0 ? x : 0.f;
+            }
+          }
+#pragma unroll
+          for (int tt = 1; tt < (NW > 0 ? NW : 1); ++tt)
+#pragma unroll
+            for (int uu = 0; uu < tt; ++uu) gp[pair_index(uu, tt)] += ew[uu] * ew[tt];
         }
       }
     }
@@ -808,29 +816,40 @@ struct Epi {
     epi_sync<NWG>(bar_id);
     const uint32_t head_id = (uint32_t)((p.layer_id_base + ch.l) * c.kv_heads + ch.h);
     const uint32_t seq_id = (uint32_t)(p.seq_id_base + ch.s);
+    const int bs = p.block_size;
+    const int N = units_of(ch.T, bs);
 #pragma unroll
     for (int r = 0; r < R2; ++r) {
       const int t = wg + NWG * r;
       if (t >= ch.ntiles) break;
       const int j = ch.j0 + t * kTileRows + row;
-      if (j >= ch.T) continue;
+      if (bs == 1 && j >= ch.T) continue;
       const float* ap = apart() + t * NWG * kTileRows + row;
       float a;
       if (NWG == 4)
         a = (ap[0] + ap[kTileRows]) + (ap[2 * kTileRows] + ap[3 * kTileRows]);
       else
         a = ap[0] + ap[kTileRows];
-      const float ct = ctp()[t * kTileRows + row];
+      float ct = ctp()[t * kTileRows + row];
+      int u = j;                 // the decision unit: this row, or its 32-row block
+      if (bs > 1) {
+        // Eq. (1) BlockSum: a block's a and c~ are the sums over its rows, which are this
+        // warp's 32 rows; lane 0 (the block's first row) finalizes it
+        a = warp_sum(j < ch.T ? a : 0.f);
+        ct = warp_sum(j < ch.T ? ct : 0.f);
+        if (lane != 0 || j >= ch.T) continue;
+        u = j / bs;
+      }
       const float sj = a + p.lambda * ct;
-      const float ramp = (ch.T > 1) ? (float)j / (float)(ch.T - 1) : 0.f;
+      const float ramp = (N > 1) ? (float)u / (float)(N - 1) : 0.f;
       const float wj = sj + p.eps_tie * ramp;
-      const long long o = (long long)ch.slice * c.capacity + j;
+      const long long o = (long long)ch.slice * c.capacity + u;
       if (A.out.flags & kEmitA) A.out.a[o] = a;
       if (A.out.flags & kEmitC) A.out.ctilde[o] = ct;
       if (A.out.flags & kEmitW) A.out.w[o] = wj;
       if (A.out.flags & kEmitKeys) {
         uint32_t key = kForcedKey;
-        if (!(j < p.n_sink || j >= ch.T - p.n_recent))
+        if (!(u < p.n_sink || u >= N - p.n_recent))
           key = candidate_key(wj, posv[r], p, head_id, seq_id);
         A.out.keys[o] = key;
       }

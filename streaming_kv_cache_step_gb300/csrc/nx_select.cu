@@ -16,20 +16,22 @@ namespace {
 
 constexpr int kSelThreads = 1024;
 
+// Order key of every unit of every slice from caller-given weights (one thread per unit;
+// a unit's Philox position is that of its first row).
 __global__ void keys_from_w_kernel(nx_cache c, nx_params p, const float* __restrict__ w,
                                    uint32_t* __restrict__ keys, const int32_t* __restrict__ newlen) {
   const int slice = blockIdx.x;
   if (newlen[slice] < 0) return;
-  const int T = c.lens[slice];
-  const int j = blockIdx.y * blockDim.x + threadIdx.x;
-  if (j >= T) return;
+  const int N = units_of(c.lens[slice], p.block_size);
+  const int u = blockIdx.y * blockDim.x + threadIdx.x;
+  if (u >= N) return;
   int l, s, h;
   slice_coords(c, slice, l, s, h);
-  const long long o = (long long)slice * c.capacity + j;
+  const long long o = (long long)slice * c.capacity + u;
   uint32_t key = kForcedKey;
-  if (!(j < p.n_sink || j >= T - p.n_recent)) {
+  if (!(u < p.n_sink || u >= N - p.n_recent)) {
     const uint32_t head_id = (uint32_t)((p.layer_id_base + l) * c.kv_heads + h);
-    key = candidate_key(w[o], c.pos[row_of(c, l, s, h, j)], p, head_id,
+    key = candidate_key(w[o], c.pos[row_of(c, l, s, h, u * p.block_size)], p, head_id,
                         (uint32_t)(p.seq_id_base + s));
   }
   keys[o] = key;
@@ -101,14 +103,17 @@ __device__ __forceinline__ void digit_hist(const uint32_t* keys, int T, uint32_t
 template <bool SMEM>
 __global__ void __launch_bounds__(kSelThreads)
 select_kernel(nx_cache c, const uint32_t* __restrict__ keys, int32_t* __restrict__ keep,
-              const int32_t* __restrict__ newlen) {
+              const int32_t* __restrict__ newlen, int bs) {
   extern __shared__ __align__(16) uint32_t s_keys[];
   grid_dep_trigger();
   grid_dep_wait();                 // keys and new lengths come from the kernels before
   const int slice = blockIdx.x;
-  const int nl = newlen[slice];
-  if (nl < 0) return;
-  const int T = c.lens[slice];
+  const int rows_left = newlen[slice];
+  if (rows_left < 0) return;
+  // decision units: the slice's T units, of which nl are kept (the new length in rows
+  // covers nl units: whole ones and the newest, possibly partial, block)
+  const int T = units_of(c.lens[slice], bs);
+  const int nl = units_of(rows_left, bs);
   int32_t* out = keep + (long long)slice * c.capacity;
   if (T <= nl) {
     for (int j = threadIdx.x; j < T; j += blockDim.x) out[j] = j;
@@ -256,7 +261,8 @@ cudaError_t launch_keys_from_w(const nx_cache& c, const nx_params& p, const floa
 }
 
 cudaError_t launch_select(const nx_cache& c, const uint32_t* keys, int32_t* keep,
-                          const int32_t* newlen, cudaStream_t st, int* launches) {
+                          const int32_t* newlen, int block_size, cudaStream_t st,
+                          int* launches) {
   const long long slices = (long long)c.layers * c.seqs * c.kv_heads;
   // keys of a slice in shared memory when they fit (up to 48K slots), else from L2
   constexpr int kSmemKeys = 48 * 1024;
@@ -273,11 +279,13 @@ cudaError_t launch_select(const nx_cache& c, const uint32_t* keys, int32_t* keep
       attr_set[dev].store(true, std::memory_order_release);
     }
     const cudaError_t e = launch_after(select_kernel<true>, dim3((unsigned)slices),
-                                       dim3(kSelThreads), bytes, st, c, keys, keep, newlen);
+                                       dim3(kSelThreads), bytes, st, c, keys, keep, newlen,
+                                       block_size);
     if (e != cudaSuccess) return e;
   } else {
     const cudaError_t e = launch_after(select_kernel<false>, dim3((unsigned)slices),
-                                       dim3(kSelThreads), 0, st, c, keys, keep, newlen);
+                                       dim3(kSelThreads), 0, st, c, keys, keep, newlen,
+                                       block_size);
     if (e != cudaSuccess) return e;
   }
   note_launch(st, launches, "select");

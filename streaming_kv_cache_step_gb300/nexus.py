@@ -52,7 +52,9 @@ class CParams(ctypes.Structure):
                 ("window", "walk_len", "n_sink", "n_recent", "n_avg", "mode")] + [
         ("lam", ctypes.c_float), ("eps_tie", ctypes.c_float), ("budget", ctypes.c_void_p),
         ("budget_max", ctypes.c_int32), ("seq_id_base", ctypes.c_int32),
-        ("layer_id_base", ctypes.c_int32), ("step", ctypes.c_uint32), ("seed", ctypes.c_uint64)]
+        ("layer_id_base", ctypes.c_int32), ("step", ctypes.c_uint32), ("seed", ctypes.c_uint64),
+        ("block_size", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("slice_budget", ctypes.c_void_p)]
 
 
 _lib = None
@@ -212,6 +214,8 @@ class Cache:
 
 @dataclass
 class Params:
+    """Step parameters (nx_params). Budgets and forced counts are in decision units:
+    rows at block_size 1, blocks of 32 rows at block_size 32."""
     budget: torch.Tensor           # int32 [seqs] on the device
     budget_max: int
     window: int
@@ -226,14 +230,20 @@ class Params:
     step: int = 0
     seq_id_base: int = 0
     layer_id_base: int = 0
+    block_size: int = 1
+    slice_budget: torch.Tensor | None = None   # int32 [slices] on the device (optional)
 
     def c_struct(self) -> CParams:
         if self.budget.dtype != torch.int32 or not self.budget.is_cuda:
             raise ValueError("budget must be an int32 CUDA tensor")
+        sb = self.slice_budget
+        if sb is not None and (sb.dtype != torch.int32 or not sb.is_cuda):
+            raise ValueError("slice_budget must be an int32 CUDA tensor")
         return CParams(self.window, self.walk_len, self.n_sink, self.n_recent, self.n_avg,
                        self.mode, self.lam, self.eps_tie, self.budget.data_ptr(),
                        self.budget_max, self.seq_id_base, self.layer_id_base,
-                       self.step & 0xFFFFFFFF, self.seed & 0xFFFFFFFFFFFFFFFF)
+                       self.step & 0xFFFFFFFF, self.seed & 0xFFFFFFFFFFFFFFFF,
+                       self.block_size, 0, None if sb is None else sb.data_ptr())
 
 
 def _check(status: int, where: str):

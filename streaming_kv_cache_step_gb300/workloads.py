@@ -138,6 +138,9 @@ class Workload:
     philox_seed: int = PHILOX_SEED
     lam: float = 0.5
     eps_tie: float = 1e-6
+    n_avg: int = 1               # reservoir averaging count n of Eq. (6)
+    block_size: int = 1          # b: rows per keep/evict decision (budgets count blocks)
+    slice_budget: np.ndarray | None = None   # int32 [L*S*Hkv]: per-slice budgets (optional)
 
     @property
     def n_slices(self) -> int:
@@ -477,8 +480,9 @@ def slice_numpy_cache(wl: Workload, sid: int, positions=None, step: int = 0,
                  k=k, v=v, pos=pos, lens=np.array([[[T]]], np.int32))
     qn = storage_to_numpy(to_storage(torch.as_tensor(query_rows(wl, sid, step)), wl.dtype))
     qn = qn.reshape(1, 1, wl.group, wl.window, wl.head_dim)
+    B = wl.budget[s] if wl.slice_budget is None else wl.slice_budget[sid]
     over = dict(seq_id_base=s, layer_id_base=layer * wl.kv_heads + h,
-                budget=np.array([wl.budget[s]], np.int32))
+                budget=np.array([B], np.int32))
     return cache, qn, over
 
 

@@ -27,11 +27,15 @@ class GpuRun:
         self.d = W.make_cache(wl, self.dev)
         self.q = W.queries(wl, step, self.dev)
         self.cache = nexus.Cache.from_dict(self.d)
+        sb = None if wl.slice_budget is None else torch.as_tensor(
+            wl.slice_budget.astype(np.int32), device=self.dev)
+        bmax = int(wl.budget.max() if sb is None else wl.slice_budget.max())
         self.params = nexus.Params(
-            budget=self.d["budget"], budget_max=int(wl.budget.max()), window=wl.window,
+            budget=self.d["budget"], budget_max=bmax, window=wl.window,
             walk_len=wl.walk_len if walk_len is None else walk_len, n_sink=wl.n_sink,
             n_recent=wl.n_recent, mode=mode, lam=wl.lam, eps_tie=wl.eps_tie,
-            seed=wl.philox_seed, step=step)
+            seed=wl.philox_seed, step=step, n_avg=wl.n_avg, block_size=wl.block_size,
+            slice_budget=sb)
         self.ws = nexus.alloc_workspace(self.cache, self.params)
         self.status = nexus.new_status(self.dev)
         S, cap = self.cache.n_slices, wl.capacity
@@ -63,7 +67,8 @@ class GpuRun:
 def oracle_params(wl: W.Workload, over: dict, mode=oracle.RESERVOIR, walk_len=None, step=0):
     return dict(window=wl.window, walk_len=wl.walk_len if walk_len is None else walk_len,
                 n_sink=wl.n_sink, n_recent=wl.n_recent, mode=mode, lam=wl.lam,
-                eps_tie=wl.eps_tie, seed=wl.philox_seed, step=step, **over)
+                eps_tie=wl.eps_tie, seed=wl.philox_seed, step=step, n_avg=wl.n_avg,
+                block_size=wl.block_size, **over)
 
 
 def oracle_slice(wl: W.Workload, sid: int, mode=oracle.RESERVOIR, walk_len=None, step=0):
@@ -91,10 +96,21 @@ def compare_survivors(gpu_keep: np.ndarray, ref_keep: np.ndarray, kappa_ref: np.
     return inter / max(n, 1)
 
 
+def slice_budget(wl, sid) -> int:
+    s = wl.slice_coords(sid)[1]
+    return int(wl.budget[s] if wl.slice_budget is None else wl.slice_budget[sid])
+
+
+def unit_positions(pos, b):
+    """Philox positions of the decision units: a block's is its first row's."""
+    return np.ascontiguousarray(pos[::b])
+
+
 def oracle_kappa(wl, sid, w32, pos, step=0, mode=oracle.RESERVOIR):
-    """Keys of every slot (NaN for forced) from the oracle's own weights."""
+    """Keys of every unit (NaN for forced) from the oracle's own weights (w32 per unit,
+    pos per row)."""
     layer, s, h = wl.slice_coords(sid)
-    T = w32.size
-    _, kappa = oracle.select_slice(w32, pos, int(wl.budget[s]), wl.n_sink, wl.n_recent, mode,
-                                   wl.philox_seed, step, layer * wl.kv_heads + h, s)
+    _, kappa = oracle.select_slice(w32, unit_positions(pos, wl.block_size), slice_budget(wl, sid),
+                                   wl.n_sink, wl.n_recent, mode, wl.philox_seed, step,
+                                   layer * wl.kv_heads + h, s, n_avg=wl.n_avg)
     return kappa

@@ -51,7 +51,7 @@ def _structs(**over):
              pos=0x30000, lens=0x40000, block_table=None)
     p = dict(window=32, walk_len=3, n_sink=32, n_recent=32, n_avg=1, mode=0, lam=0.5,
              eps_tie=1e-6, budget=0x50000, budget_max=1638, seq_id_base=0, layer_id_base=0,
-             step=0, seed=1)
+             step=0, seed=1, block_size=1, reserved=0, slice_budget=None)
     for k, v in over.items():
         (c if k in c else p)[k] = v
     cc = nexus.CCache(*[c[n] for n, _ in nexus.CCache._fields_])
@@ -66,10 +66,17 @@ def test_workspace_bytes_and_validation(lib):
     bad = [dict(head_dim=96), dict(window=0), dict(window=65), dict(walk_len=33),
            dict(walk_len=9), dict(k=0x10008), dict(budget_max=63), dict(budget_max=9000),
            dict(page_size=12), dict(dtype=7), dict(seq_id_base=(1 << 24) - 1),
-           dict(lam=-1.0), dict(n_avg=0), dict(n_avg=5)]
+           dict(lam=-1.0), dict(n_avg=0), dict(n_avg=1025), dict(block_size=0),
+           dict(block_size=16), dict(block_size=32, budget_max=257),
+           dict(block_size=32, n_sink=1, n_recent=0, budget_max=100), dict(reserved=1)]
     for b in bad:
         c, p = _structs(**b)
         assert lib.nexus_workspace_bytes(ctypes.byref(c), ctypes.byref(p)) == 0, b
+    # the paper's n = 5 and b = 32 (budgets in blocks: 8192 rows hold 256 blocks)
+    for good in (dict(n_avg=5), dict(n_avg=1024),
+                 dict(block_size=32, n_sink=1, n_recent=1, budget_max=52)):
+        c, p = _structs(**good)
+        assert lib.nexus_workspace_bytes(ctypes.byref(c), ctypes.byref(p)) > 0, good
 
 
 def test_entry_points_reject_before_touching_the_gpu(lib):
@@ -79,7 +86,7 @@ def test_entry_points_reject_before_touching_the_gpu(lib):
     ws, st = P(0x100000), P(0x200000)
     assert lib.nexus_evict_step(ctypes.byref(c), P(0x60000), ctypes.byref(p), None, ws,
                                 1 << 40, st, None) == nexus.NX_ERR_INVALID_ARG
-    c, p = _structs(n_avg=5)
+    c, p = _structs(block_size=16, n_sink=1, n_recent=1, budget_max=100)
     assert lib.nexus_evict_step(ctypes.byref(c), P(0x60000), ctypes.byref(p), None, ws,
                                 1 << 40, st, None) == nexus.NX_ERR_UNSUPPORTED
     c, p = _structs()

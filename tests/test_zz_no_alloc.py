@@ -78,7 +78,7 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     lib.kv_compact_noalloc.restype = ctypes.c_int
     c = nexus.CCache(1, 512, 8, 4, 128, 32768, 0, 0, 0, nexus.DTYPE_BF16, 1 << 20, 1 << 21,
                      1 << 22, 1 << 23, None)
-    p = nexus.CParams(32, 3, 32, 32, 1, 0, 0.5, 1e-6, 1 << 24, 26214, 0, 0, 0, 1)
+    p = nexus.CParams(32, 3, 32, 32, 1, 0, 0.5, 1e-6, 1 << 24, 26214, 0, 0, 0, 1, 1, 0, None)
     rc = lib.kv_compact_noalloc(ctypes.byref(c), ctypes.c_void_p(1 << 25), ctypes.byref(p),
                                 ctypes.c_void_p(1 << 26), None)
     assert rc == nexus.NX_ERR_WORKSPACE
