@@ -58,6 +58,11 @@ def parse_args():
     ap.add_argument("--workload", default="batch16_32layers")
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--n-avg", type=int, default=1,
+                    help="reservoir averaging count n of Eq. (6) (the paper runs n = 5)")
+    ap.add_argument("--block-size", type=int, default=1, choices=(1, 32),
+                    help="rows per keep/evict decision; at 32 the workload's budget becomes "
+                         "ceil(B / 32) blocks with one sink and one recency block")
     ap.add_argument("--launch", choices=("graph", "eager"), default="graph",
                     help="device-timed loop: replay one CUDA-graph capture of the "
                          "nexus_evict_step call, or call it eagerly every step")
@@ -215,19 +220,42 @@ def job_rate(rows_per_step: int, steps: int, local_ms: float, world: int) -> tup
 # ---------------------------------------------------------------------------
 
 def algorithmic_bytes(wl, lens0: np.ndarray, keep: np.ndarray, newlen: np.ndarray) -> dict:
-    """Per step: K read once + pos (scoring), queries, the kept-slot list, and every
-    moved row's k, v and pos read and written (compaction)."""
+    """Per step: K read once + pos (scoring), queries, the kept-unit list, and every
+    moved row's k, v and pos read and written (compaction). keep holds kept units (rows,
+    or blocks of wl.block_size rows); newlen the rows left per slice."""
     eb = 2 if wl.dtype == "bf16" else 4
     row = wl.head_dim * eb
+    b = wl.block_size
     rows = int(lens0.sum())
-    moved = 0
+    moved, units = 0, 0
     for i in range(keep.shape[0]):
         n = int(newlen[i])
-        moved += int((keep[i, :n] != np.arange(n)).sum())
+        nu = -(-n // b)
+        units += nu
+        u = keep[i, :nu]
+        if b == 1:
+            moved += int((u != np.arange(nu)).sum())
+        else:
+            # a block moves whole; the newest block may hold fewer than b rows
+            sizes = np.minimum(b, int(lens0[i]) - u * b)
+            moved += int(sizes[u != np.arange(nu)].sum())
     qbytes = wl.n_slices * wl.group * wl.window * wl.head_dim * eb
     score = rows * (row + 4) + qbytes
-    compact = moved * (4 * row + 8) + int(newlen.sum()) * 4
+    compact = moved * (4 * row + 8) + units * 4
     return dict(rows=rows, moved=moved, score=score, compact=compact, total=score + compact)
+
+
+def configured_workload(args):
+    """The named workload with the reservoir averaging count and block size asked for."""
+    import dataclasses
+    from streaming_kv_cache_step_gb300 import workloads as W
+    wl = W.WORKLOADS[args.workload]()
+    over = dict(n_avg=getattr(args, "n_avg", 1))
+    b = getattr(args, "block_size", 1)
+    if b > 1:
+        over.update(block_size=b, n_sink=-(-wl.n_sink // b), n_recent=-(-wl.n_recent // b),
+                    budget=(-(-wl.budget // b)).astype(np.int32))
+    return dataclasses.replace(wl, **over)
 
 
 # ---------------------------------------------------------------------------
@@ -250,7 +278,7 @@ def run_native(args, rank, world, local):
     _log("library built and loaded")
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    wl = W.WORKLOADS[args.workload]()
+    wl = configured_workload(args)
     pristine = W.make_cache(wl, dev)
     _log(f"cache of {wl.name} generated on the device")
     work = {k: (v.clone() if torch.is_tensor(v) else v) for k, v in pristine.items()}
@@ -259,7 +287,8 @@ def run_native(args, rank, world, local):
     params = nexus.Params(budget=work["budget"], budget_max=int(wl.budget.max()),
                           window=wl.window, walk_len=wl.walk_len, n_sink=wl.n_sink,
                           n_recent=wl.n_recent, lam=wl.lam, eps_tie=wl.eps_tie,
-                          seed=wl.philox_seed, step=0, seq_id_base=rank_seq_base(rank, wl))
+                          seed=wl.philox_seed, step=0, seq_id_base=rank_seq_base(rank, wl),
+                          n_avg=wl.n_avg, block_size=wl.block_size)
     ws = nexus.alloc_workspace(cache, params)
     status = nexus.new_status(dev)
     keep = torch.full((cache.n_slices, wl.capacity), -1, dtype=torch.int32, device=dev)
@@ -439,7 +468,8 @@ def run_native(args, rank, world, local):
                            q_heads=wl.q_heads, kv_heads=wl.kv_heads, head_dim=wl.head_dim,
                            cache_rows=int(wl.lens.max()), budget=int(wl.budget.max()),
                            window=wl.window, walk=wl.walk_len, n_sink=wl.n_sink,
-                           n_recent=wl.n_recent, rows_per_step=rows_per_step,
+                           n_recent=wl.n_recent, n_avg=wl.n_avg, block_size=wl.block_size,
+                           rows_per_step=rows_per_step,
                            moved_rows=ab["moved"], alg_bytes_per_step=ab["total"],
                            l2="flushed between timed steps (2x L2 written, then 2x L2 read)",
                            launch=("one CUDA-graph capture of the nexus_evict_step call, "
@@ -479,7 +509,7 @@ def _oracle_pass(wl, slices, pool):
         cc = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in c.items()}
         pr = dict(window=wl.window, walk_len=wl.walk_len, n_sink=wl.n_sink,
                   n_recent=wl.n_recent, lam=wl.lam, eps_tie=wl.eps_tie, seed=wl.philox_seed,
-                  step=0, **over)
+                  step=0, n_avg=wl.n_avg, block_size=wl.block_size, **over)
         oracle.evict_step(cc, q, pr, mutate=True, nthreads=1)
         return int(c["lens"].reshape(-1)[0])
 
@@ -519,7 +549,7 @@ def run_reference(args, rank, world):
         return None
     import oracle
     oracle.build()
-    wl = W.WORKLOADS[args.workload]()
+    wl = configured_workload(args)
     cores = os.cpu_count() or 1
     slices = _oracle_slices(wl, cores)
     with ThreadPoolExecutor(max_workers=len(slices)) as pool:

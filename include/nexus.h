@@ -297,10 +297,17 @@ const char* nx_status_string(nx_status status);
  *                          it was rejected before launching anything);
  *   NX_SCORER_TENSOR_CORE  the tcgen05 scorer, which reads every cached key once;
  *   NX_SCORER_CUDA_CORE    the CUDA-core scorer (fp32 caches, shapes the tensor-core
- *                          scorer does not cover), which reads every cached key twice.
+ *                          scorer does not cover), which reads every cached key twice;
+ *   NX_SCORER_TENSOR_CORE_TWO_PASS  the tcgen05 scorer in two launches, used when a
+ *                          slice is longer than the single pass holds on chip at once
+ *                          (152 SMs x 8 tiles x 128 rows = 155,648 rows on a GB300,
+ *                          e.g. a one-shot eviction at the end of a long prefill):
+ *                          the first stores every chunk's softmax record, the second
+ *                          recomputes the logits and finishes; every key is read twice.
  * The results are the same within the score tolerance either way.
  */
-enum { NX_SCORER_NONE = 0, NX_SCORER_TENSOR_CORE = 1, NX_SCORER_CUDA_CORE = 2 };
+enum { NX_SCORER_NONE = 0, NX_SCORER_TENSOR_CORE = 1, NX_SCORER_CUDA_CORE = 2,
+       NX_SCORER_TENSOR_CORE_TWO_PASS = 3 };
 int32_t nexus_last_scorer(void);
 
 /* Kernels launched by the most recent call made from this host thread. */

@@ -145,11 +145,11 @@ cudaError_t run_scores(const nx_cache& c, const void* q, const nx_params& p, con
   cudaError_t e = launch_prep(c, q, p, L, ws, dev_status, st, launches, tc ? 2 : 1);
   if (e != cudaSuccess) return e;
   if (tc) {
-    bool used = false;
-    e = launch_score_tc(c, p, q, L, ws, out, dev_status, st, launches, &used);
+    bool used = false, two_pass = false;
+    e = launch_score_tc(c, p, q, L, ws, out, dev_status, st, launches, &used, &two_pass);
     if (e != cudaSuccess) return e;
     if (used) {
-      g_last_scorer = NX_SCORER_TENSOR_CORE;
+      g_last_scorer = two_pass ? NX_SCORER_TENSOR_CORE_TWO_PASS : NX_SCORER_TENSOR_CORE;
       return e;
     }
     // not launchable for this size: the CUDA-core path needs the fp32 queries

@@ -334,7 +334,8 @@ void tc_set_layout(int teams);
 void tc_last_config(int32_t* out);
 cudaError_t launch_score_tc(const nx_cache& c, const nx_params& p, const void* q,
                             const WsLayout& L, char* ws, const ScoreOut& out,
-                            int32_t* dev_status, cudaStream_t st, int* launches, bool* used);
+                            int32_t* dev_status, cudaStream_t st, int* launches, bool* used,
+                            bool* two_pass);
 cudaError_t launch_score_simt(const nx_cache& c, const nx_params& p, const WsLayout& L, char* ws,
                               const ScoreOut& out, int32_t* dev_status, cudaStream_t st,
                               int* launches);

@@ -81,6 +81,10 @@ struct Args {
   int stride;              // floats per partial record
   long long total_ids;     // slices * maxc
   int slices;
+  // 0: one pass (chunk records merged across CTAs through the slice barrier);
+  // 1: records only (each TMEM buffer is freed once its chunk's record is stored);
+  // 2: the pass after 1: the records are complete, nothing waits on another CTA
+  int pass;
 };
 
 // ---------------------------------------------------------------------------
@@ -658,7 +662,9 @@ struct Epi {
       }
     }
     epi_sync<NWG>(bar_id);
+    // (the pass after a records-only pass stores nothing: its records are the same bits)
     float* rec = A.partial + ((long long)ch.slice * A.maxc + ch.k) * A.stride;
+    const bool store = A.pass != 2;
     const float* mwb = mw(ch.b);
     if (tid < W) {
       const int col = tid, g = col / CW;
@@ -672,9 +678,11 @@ struct Epi {
 #pragma unroll
       for (int q = 0; q < 4; ++q) x += red()[(4 * g + q) * RS + col] * exp2f((mq[q] - mm) * cl2);
       m[col] = mm;
-      rec[col] = mm;                      // chunk max (raw)
-      rec[W + col] = x;                   // sum relative to it
-    } else if (tid < W + kMaxPairs) {
+      if (store) {
+        rec[col] = mm;                    // chunk max (raw)
+        rec[W + col] = x;                 // sum relative to it
+      }
+    } else if (store && tid < W + kMaxPairs) {
       const int k = tid - W;
       int u = 0, t = 0;
       pair_of(k, u, t);
@@ -900,6 +908,13 @@ struct Epi {
       if (tid == 0) trace_ev(A, vcta, nev, 2 + 1000 * (ch.slice + 1));
       publish(ch, ok, bar_pub);
       if (!ok) break;
+      if (A.pass == 1) {
+        // records only: the chunk's TMEM buffer is free as soon as its record is stored
+        tc_fence_before();
+        epi_sync<NWG>(bar_id);
+        if (tid == 0) mbar_arrive(&bar_tempty[ch.b]);
+        continue;
+      }
       if (nbuf == 1) {
         if (!finish(ch)) break;
       } else {
@@ -931,6 +946,7 @@ __device__ void merge_warp(const Args& A, uint8_t* sm, int chunk_rows, int nbuf,
   float* stage = reinterpret_cast<float*>(sm + S::kOffStage);
   float* ms = reinterpret_cast<float*>(sm + S::kOffMs);     // [0]: maxima, [1]: normalisers
   uint32_t cnt = 0, htx = 0;
+  if (A.pass == 1) return;                 // records only: nothing to merge
   Sched sc;
   sched_init(sc, vcta, vgrid);
   int sl, kq, Tq;
@@ -938,8 +954,9 @@ __device__ void merge_warp(const Args& A, uint8_t* sm, int chunk_rows, int nbuf,
     const Chunk ch = make_chunk(A, sl, kq, Tq, chunk_rows, cnt, nbuf);
     int ok = 1;
     if (lane == 0) {
+      // after a records-only pass every record of the slice is already in memory
       ok = mbar_wait(&bar_tempty[ch.b], (ch.use & 1) ^ 1, A.dev_status) &&
-           wait_at_least(&A.arrive[ch.slice], ch.nchunks, A.dev_status);
+           (A.pass == 2 || wait_at_least(&A.arrive[ch.slice], ch.nchunks, A.dev_status));
       __threadfence();
       // the records were written through the generic proxy; the bulk copies read them
       // through the async proxy
@@ -1307,7 +1324,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 template <int W, int D, int NWG>
 cudaError_t launch_t(const nx_cache& c, const nx_params& p, const void* q, const WsLayout& L,
                      char* ws, const ScoreOut& out, int32_t* dev_status, cudaStream_t st,
-                     int* launches, bool* used) {
+                     int* launches, bool* used, bool* two_pass) {
   using S = Smem<W, D, NWG>;
   using R = Roles<NWG>;
   *used = false;
@@ -1401,7 +1418,18 @@ cudaError_t launch_t(const nx_cache& c, const nx_params& p, const void* q, const
         }
       }
     }
-    if (!nbuf) { g_last_cfg[0] = -4; return cudaSuccess; }
+    // A slice with more chunks than there are co-resident pipelines cannot wait for its
+    // own records at the slice barrier: two passes then, the first storing every chunk's
+    // record, the second (which waits on no other CTA) recomputing the logits and
+    // finishing against the complete records. K is read twice.
+    int passes = 1;
+    if (!nbuf) {
+      passes = 2;
+      nbuf = 2;
+      tpc = min(R::kMaxChunkTiles, (int)(tmem_cols / 2 / W));
+      maxc = (int)((cap_tiles + tpc - 1) / tpc);
+      grid_sel = grid_max;
+    }
     Args a;
     a.c = c;
     a.p = p;
@@ -1423,31 +1451,35 @@ cudaError_t launch_t(const nx_cache& c, const nx_params& p, const void* q, const
     const long long vgrid = a.total_ids < grid_sel ? a.total_ids : grid_sel;
     const long long grid = (vgrid + R::kTeams - 1) / R::kTeams;  // CTAs of kTeams teams
 
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(R::kBlockThreads);
-    cfg.dynamicSmemBytes = S::kAlloc;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, score_tc_kernel<W, D, NWG>, map, a);
-    if (e == cudaErrorInvalidValue || e == cudaErrorNotSupported) {
-      (void)cudaGetLastError();            // without the early start, then
-      cfg.numAttrs = 1;
-      e = cudaLaunchKernelEx(&cfg, score_tc_kernel<W, D, NWG>, map, a);
+    for (int pass = (passes == 1 ? 0 : 1); pass <= (passes == 1 ? 0 : 2); ++pass) {
+      a.pass = pass;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)grid);
+      cfg.blockDim = dim3(R::kBlockThreads);
+      cfg.dynamicSmemBytes = S::kAlloc;
+      cfg.stream = st;
+      cudaLaunchAttribute attr[2];
+      attr[0].id = cudaLaunchAttributeCooperative;
+      attr[0].val.cooperative = 1;
+      attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[1].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 2;
+      cudaError_t e = cudaLaunchKernelEx(&cfg, score_tc_kernel<W, D, NWG>, map, a);
+      if (e == cudaErrorInvalidValue || e == cudaErrorNotSupported) {
+        (void)cudaGetLastError();            // without the early start, then
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, score_tc_kernel<W, D, NWG>, map, a);
+      }
+      if (e == cudaErrorCooperativeLaunchTooLarge && pass <= 1) {
+        (void)cudaGetLastError();
+        g_last_cfg[0] = -5;
+        g_last_cfg[1] = per_sm_api;
+        return cudaSuccess;
+      }
+      if (e != cudaSuccess) return e;
+      note_launch(st, launches, pass == 1 ? "score_tc_records" : "score_tc");
     }
-    if (e == cudaErrorCooperativeLaunchTooLarge) {
-      (void)cudaGetLastError();
-      g_last_cfg[0] = -5;
-      g_last_cfg[1] = per_sm_api;
-      return cudaSuccess;
-    }
-    if (e != cudaSuccess) return e;
     g_last_cfg[0] = R::kTeams;
     (void)per_sm;
     g_last_cfg[1] = per_sm_api;
@@ -1457,8 +1489,8 @@ cudaError_t launch_t(const nx_cache& c, const nx_params& p, const void* q, const
     g_last_cfg[5] = maxc;
     g_last_cfg[6] = (int32_t)tmem_cols;
     g_last_cfg[7] = S::kAlloc;
-    note_launch(st, launches, "score_tc");
     *used = true;
+    *two_pass = passes == 2;
     return cudaSuccess;
   }
   return cudaSuccess;
@@ -1483,12 +1515,14 @@ bool tc_supported(const nx_cache& c, const nx_params& p) {
 
 cudaError_t launch_score_tc(const nx_cache& c, const nx_params& p, const void* q,
                             const WsLayout& L, char* ws, const ScoreOut& out,
-                            int32_t* dev_status, cudaStream_t st, int* launches, bool* used) {
+                            int32_t* dev_status, cudaStream_t st, int* launches, bool* used,
+                            bool* two_pass) {
   *used = false;
+  *two_pass = false;
   if (!tc_supported(c, p)) return cudaSuccess;
   const bool d128 = c.head_dim == 128;
 #define NX_TC_LAUNCH(WW, DD, NN) \
-  tc::launch_t<WW, DD, NN>(c, p, q, L, ws, out, dev_status, st, launches, used)
+  tc::launch_t<WW, DD, NN>(c, p, q, L, ws, out, dev_status, st, launches, used, two_pass)
   // Windows of up to 32 rows may take two pipelines per CTA. Automatic choice: two for large
   // paged caches (one TMA copy per page: two producers keep more of them in flight), one
   // otherwise (measured faster for contiguous caches); a layout that cannot run falls back.

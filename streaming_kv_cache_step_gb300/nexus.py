@@ -30,7 +30,7 @@ SYMBOLS = ("nexus_workspace_bytes", "nexus_direct_scores", "nexus_walk",
            "nexus_profile_next_call", "nexus_debug_force_simt", "nexus_debug_set_trace",
            "nexus_debug_scorer_config", "nexus_debug_scorer_layout", "kv_compact_noalloc",
            "nexus_last_scorer")
-SCORER_NONE, SCORER_TENSOR_CORE, SCORER_CUDA_CORE = 0, 1, 2
+SCORER_NONE, SCORER_TENSOR_CORE, SCORER_CUDA_CORE, SCORER_TENSOR_CORE_TWO_PASS = 0, 1, 2, 3
 
 
 class NexusError(RuntimeError):

@@ -27,6 +27,7 @@ The recipes follow the workloads the eviction step is measured on:
   norms and 256 planted query->hub->bridge chains.
 * streaming_paged: 256 ragged sequences with 16-token pages, evicted every
   decode token.
+* prefill_256k: a one-shot eviction at the end of a 262144-token prefill.
 
 Each recipe is described in full where it is defined below.
 """
@@ -548,6 +549,18 @@ def streaming_paged(n_seqs: int = 256) -> Workload:
                     query_gain=2.0, seed=DATA_SEED_BASE + 4)
 
 
+def prefill_256k() -> Workload:
+    """One-shot eviction at the end of a long prefill (the paper's §2.1 streaming view: a
+    long prompt can trigger one eviction when prefill ends): 2 sequences x 8 kv heads
+    (32 q heads), d = 128 bf16, 262144 prompt tokens per slice, the window being the last
+    32 prompt rows, H = 3, keep 20% (B = 52428), one step; 64 Zipf(1.1) hubs per head as
+    in the Llama layer. Longer than one on-chip pass of the tensor-core scorer."""
+    return Workload(name="prefill_256k", layers=1, seqs=2, kv_heads=8, group=4, head_dim=128,
+                    dtype="bf16", lens=np.full(2, 262144, np.int32), capacity=262144,
+                    window=32, walk_len=3, budget=np.full(2, 52428, np.int32), steps=1,
+                    n_hubs=64, query_gain=8.0, zipf=1.1, seed=DATA_SEED_BASE + 5)
+
+
 def batch16_1layer() -> Workload:
     """One layer of the 16-sequence batch (128 slices, 1 GiB of keys): a profiling case
     larger than L2 that a counter capture replays quickly."""
@@ -560,6 +573,7 @@ WORKLOADS = {
     "batch16_32layers": batch16_32layers,
     "long_context": long_context,
     "streaming_paged": streaming_paged,
+    "prefill_256k": prefill_256k,
     "batch16_1layer": batch16_1layer,
 }
 

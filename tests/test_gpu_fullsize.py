@@ -43,7 +43,8 @@ def _check_all_slices(run, keep, lens0):
             assert np.array_equal(k[nl - wl.n_recent:], np.arange(T - wl.n_recent, T))
 
 
-FULL = {"llama3_8b_layer": 8, "batch16_32layers": 10, "long_context": 3, "streaming_paged": 10}
+FULL = {"llama3_8b_layer": 8, "batch16_32layers": 10, "long_context": 3, "streaming_paged": 10,
+        "prefill_256k": 2}
 
 
 @pytest.mark.parametrize("name", list(FULL))

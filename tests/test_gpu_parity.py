@@ -434,29 +434,35 @@ def test_select_reservoir_with_zero_weights_bitexact():
     _select_on_given_weights(TIES, w, nexus.MODE_RESERVOIR)
 
 
-def test_slice_beyond_the_tensor_core_residency_limit():
-    # One slice longer than the tensor-core scorer's co-resident chunks hold (152 pipelines
-    # x 8 tiles x 128 rows): the call still gives the oracle's results, and reports which
-    # scorer it used.
-    T = 160_000
-    wl = W.shrink(W.llama3_8b_layer(), seqs=1, kv_heads=1, lens=np.array([T], np.int32),
-                  capacity=T, budget=np.array([T // 5], np.int32), n_hubs=16)
+@pytest.mark.parametrize("lens,window", [((160_000,), 32), ((170_000, 3000), 32),
+                                         ((158_000,), 64), ((157_000,), 16)])
+def test_slices_beyond_the_single_pass_residency_limit(lens, window):
+    # Slices longer than the single tensor-core pass holds on chip (152 pipelines x 8 tiles x
+    # 128 rows) take the two-pass tensor-core scorer (records first, then the finish): the
+    # results are the oracle's, and the call says which scorer it used.
+    lens = np.array(lens, np.int32)
+    cap = int(lens.max())
+    wl = W.shrink(W.llama3_8b_layer(), seqs=lens.size, kv_heads=1, lens=lens, capacity=cap,
+                  budget=(lens // 5).astype(np.int32), n_hubs=16, window=window,
+                  walk_len=5 if window == 64 else 3)
     run = GpuRun(wl)
-    w = torch.full((1, T), -1.0, device=DEV)
+    S = run.cache.n_slices
+    w = torch.full((S, cap), -1.0, device=DEV)
     nexus.walk(run.cache, run.q, run.params, w, None, run.ws, run.status)
     run.check_status()
-    scorer = nexus.last_scorer()
-    assert scorer in (nexus.SCORER_TENSOR_CORE, nexus.SCORER_CUDA_CORE)
-    print("scorer", scorer, nexus.scorer_config())
+    assert nexus.last_scorer() == nexus.SCORER_TENSOR_CORE_TWO_PASS, nexus.scorer_config()
+    assert nexus.last_launch_names()[1:3] == ["score_tc_records", "score_tc"]
     nexus.evict_step(run.cache, run.q, run.params, run.keep, run.ws, run.status)
     run.check_status()
-    assert nexus.last_scorer() == scorer
-    c, _, _, ref = oracle_slice(wl, 0)
+    assert nexus.last_scorer() == nexus.SCORER_TENSOR_CORE_TWO_PASS
     w = w.cpu().numpy()
-    assert np.all(np.abs(w[0] - ref["w"][0, :T]) <= score_tol(ref["w"][0, :T], T))
-    nl = int(ref["newlen"][0])
-    kappa = oracle_kappa(wl, 0, ref["w"][0, :T], c["pos"][0, 0, 0, :T])
     keep = run.keep.cpu().numpy()
-    compare_survivors(keep[0, :nl], ref["keep"][0, :nl], kappa)
-    got = W.storage_to_numpy(run.slice_rows("k", 0, nl))
-    assert np.array_equal(got, c["k"][0, 0, 0][keep[0, :nl]])
+    for sid in range(S):
+        T = int(lens[sid])
+        c, _, _, ref = oracle_slice(wl, sid)
+        assert np.all(np.abs(w[sid, :T] - ref["w"][0, :T]) <= score_tol(ref["w"][0, :T], T))
+        nl = int(ref["newlen"][0])
+        kappa = oracle_kappa(wl, sid, ref["w"][0, :T], c["pos"][0, 0, 0, :T])
+        compare_survivors(keep[sid, :nl], ref["keep"][0, :nl], kappa)
+        got = W.storage_to_numpy(run.slice_rows("k", sid, nl))
+        assert np.array_equal(got, c["k"][0, 0, 0][keep[sid, :nl]])
