@@ -133,6 +133,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// L2 prefetch of one tensor-map box (no shared memory, no barrier): the bytes are in L2
+// when the load of the same box is issued later.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
                                           uint64_t* bar) {
   asm volatile(
@@ -358,19 +367,23 @@ struct Smem {
 };
 
 // The chunk schedule. The chunks of all slices are numbered in slice order (a slice that
-// is empty or was rejected has none), and chunk number x goes to CTA x mod grid. As a
-// slice has at most grid chunks, a CTA holds at most one chunk of any slice, and it takes
-// its chunks in increasing slice order: that keeps the slice barrier deadlock-free (the
-// earliest unfinished slice never waits on a later one), and however ragged the lengths,
-// the CTAs' chunk counts differ by at most one. Every warp of every role walks the same
+// is empty or was rejected has none), and chunk number x goes to CTA x mod grid. In the
+// one-pass mode a slice has at most grid chunks, so a CTA holds at most one chunk of any
+// slice, and it takes its chunks in increasing slice order: that keeps the slice barrier
+// deadlock-free (the earliest unfinished slice never waits on a later one), and however
+// ragged the lengths, the CTAs' chunk counts differ by at most one. (The two-pass mode,
+// which waits on no other CTA, allows more chunks per slice than CTAs.) Every warp of every role walks the same
 // sequence itself, warp-collectively: 32 slices at a time, one per lane, with a warp
 // scan of their chunk counts.
 struct Sched {
   int cta, ncta;     // this (virtual) CTA and how many there are
   long long first;   // chunk number of the first chunk of slice `base`
   int base;          // first slice of the current batch
-  uint32_t mask;     // lanes whose slice has a chunk for this CTA
-  int k, T;          // this lane's slice: the chunk index for this CTA, its length
+  uint32_t mask;     // lanes whose slice has a chunk left for this CTA
+  int k, T, n;       // this lane's slice: the next chunk index for this CTA, its length,
+                     // its chunk count
+  int pre_nl, pre_t; // the next batch's new length and length for this lane (loaded one
+                     // batch ahead, so that a refill does not wait on global memory)
 };
 
 __device__ __forceinline__ void sched_init(Sched& S, int cta, int ncta) {
@@ -381,6 +394,9 @@ __device__ __forceinline__ void sched_init(Sched& S, int cta, int ncta) {
   S.mask = 0;
   S.k = 0;
   S.T = 0;
+  S.n = 0;
+  S.pre_nl = -2;     // nothing loaded ahead yet
+  S.pre_t = 0;
 }
 
 // Warp-collective: the next chunk of this CTA; false once there is none.
@@ -391,11 +407,21 @@ __device__ __forceinline__ bool sched_next(const Args& A, Sched& S, int chunk_ro
     S.base += 32;
     if (S.base >= A.slices) return false;
     const int sl = S.base + lane;
-    int t = 0, n = 0;
-    if (sl < A.slices && __ldg(&A.newlen[sl]) >= 0) {
+    int nl = -1, t = 0, n = 0;
+    if (S.pre_nl != -2) {
+      nl = S.pre_nl;
+      t = S.pre_t;
+    } else if (sl < A.slices) {
+      nl = __ldg(&A.newlen[sl]);
       t = __ldg(&A.c.lens[sl]);
-      n = (t + chunk_rows - 1) / chunk_rows;
     }
+    {
+      const int sl2 = sl + 32;        // load the next batch now; used at the next refill
+      S.pre_nl = sl2 < A.slices ? __ldg(&A.newlen[sl2]) : -1;
+      S.pre_t = sl2 < A.slices ? __ldg(&A.c.lens[sl2]) : 0;
+    }
+    if (sl < A.slices && nl >= 0) n = (t + chunk_rows - 1) / chunk_rows;
+    else t = 0;
     int incl = n;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -407,14 +433,19 @@ __device__ __forceinline__ bool sched_next(const Args& A, Sched& S, int chunk_ro
     if (kk < 0) kk += S.ncta;
     S.k = kk;
     S.T = t;
+    S.n = n;
     S.mask = __ballot_sync(0xffffffffu, kk < n);
     S.first += __shfl_sync(0xffffffffu, incl, 31);
   }
   const int j = __ffs(S.mask) - 1;
-  S.mask &= S.mask - 1;
   slice = S.base + j;
   k = __shfl_sync(0xffffffffu, S.k, j);
   T = __shfl_sync(0xffffffffu, S.T, j);
+  // a slice with more chunks than CTAs gives this CTA chunks k, k + ncta, ... (only in
+  // the two-pass mode, which has no slice barrier)
+  const int n_j = __shfl_sync(0xffffffffu, S.n, j);
+  if ((threadIdx.x & 31) == j) S.k += S.ncta;
+  if (k + S.ncta >= n_j) S.mask &= S.mask - 1;
   return true;
 }
 
@@ -444,6 +475,16 @@ __device__ __forceinline__ void trace_ev(const Args& A, int cta, int& n, int tag
   }
 }
 
+// the same for the MMA issuer (slots from 512) and the TMA producer (slots from 768)
+__device__ __forceinline__ void trace_role(const Args& A, int cta, int base, int& n, int tag) {
+  if (A.trace && base + n < kTraceEvents - 3 && n < 256) {
+    long long* t = A.trace + ((long long)cta * kTraceEvents + base + n) * 2;
+    t[0] = tag;
+    t[1] = global_ns();
+    ++n;
+  }
+}
+
 // kernel-level marks in the last three trace slots of the CTA: entry, setup done, exit
 __device__ __forceinline__ void trace_mark(const Args& A, int cta, int slot, int tag) {
   if (A.trace) {
@@ -462,6 +503,7 @@ struct Chunk {
   int slice, k, T, nchunks, j0, ntiles, l, s, h;
   uint32_t b;          // TMEM buffer
   uint32_t use;        // how many times this buffer was used before
+  uint32_t cnt;        // this pipeline's chunk number
 };
 
 __device__ __forceinline__ Chunk make_chunk(const Args& A, int slice, int k, int T,
@@ -476,6 +518,7 @@ __device__ __forceinline__ Chunk make_chunk(const Args& A, int slice, int k, int
   slice_coords(A.c, ch.slice, ch.l, ch.s, ch.h);
   ch.b = cc % nbuf;
   ch.use = cc / nbuf;
+  ch.cnt = cc;
   return ch;
 }
 
@@ -573,9 +616,18 @@ struct Epi {
       }
     }
     if (tid == 0) trace_ev(A, vcta, nev, 10);
+    // The publisher warp reads the previous chunk's lane-quarter partials (mw, red) to
+    // build its record; they are overwritten only once it has taken them.
+    if (ch.cnt > 0 && lane == 0) {
+      uint64_t* bar_rec =
+          reinterpret_cast<uint64_t*>(sm + Smem<W, D, NWG>::kOffBar) + 2 * Smem<W, D, NWG>::kStages + 15;
+      int* ctl = reinterpret_cast<int*>(sm + Smem<W, D, NWG>::kOffMisc + 16);
+      if (!mbar_wait(bar_rec, (ch.cnt - 1) & 1, A.dev_status)) ctl[1] = 1;
+    }
+    __syncwarp();
     // Each warp shifts its own rows by its own column maxima (no barrier here); the
-    // record step below rescales the four lane quarters to the chunk maximum, and pass 2
-    // folds the same factor into its weights.
+    // publisher warp rescales the four lane quarters to the chunk maximum for the record,
+    // and pass 2 folds the same factor into its weights.
     float* mwq = mw(ch.b) + lg * W;
 #pragma unroll
     for (int i = 0; i < CW; ++i) {
@@ -661,57 +713,89 @@ struct Epi {
         if (lane == 0) red()[warp * RS + W + i] = x;
       }
     }
-    epi_sync<NWG>(bar_id);
-    // (the pass after a records-only pass stores nothing: its records are the same bits)
-    float* rec = A.partial + ((long long)ch.slice * A.maxc + ch.k) * A.stride;
-    const bool store = A.pass != 2;
-    const float* mwb = mw(ch.b);
-    if (tid < W) {
-      const int col = tid, g = col / CW;
-      float mq[4], mm = -INFINITY;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        mq[q] = mwb[q * W + col];
-        mm = fmaxf(mm, mq[q]);
-      }
-      float x = 0.f;                      // quarter sums rescaled to the chunk maximum
-#pragma unroll
-      for (int q = 0; q < 4; ++q) x += red()[(4 * g + q) * RS + col] * exp2f((mq[q] - mm) * cl2);
-      m[col] = mm;
-      if (store) {
-        rec[col] = mm;                    // chunk max (raw)
-        rec[W + col] = x;                 // sum relative to it
-      }
-    } else if (store && tid < W + kMaxPairs) {
-      const int k = tid - W;
-      int u = 0, t = 0;
-      pair_of(k, u, t);
-      float x = 0.f;
-      if (t < H) {
-        const int cp = W - H + u, cq = W - H + t;
-        float mp = -INFINITY, mq = -INFINITY;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          mp = fmaxf(mp, mwb[q * W + cp]);
-          mq = fmaxf(mq, mwb[q * W + cq]);
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          x += red()[(4 * kWalkWg + q) * RS + W + k] *
-               exp2f(((mwb[q * W + cp] - mp) + (mwb[q * W + cq] - mq)) * cl2);
-      }
-      rec[2 * W + k] = x;                 // Gram entry
-    }
   }
 
-  // Hand the chunk's record to the publisher warp: each epilogue warp arrives once its
-  // stores are issued (the arrive orders them before the publisher's fence).
+  // Hand the chunk's partials to the publisher warp: each epilogue warp arrives once its
+  // shared-memory stores are issued (the arrive releases them to the publisher).
   __device__ void publish(const Chunk& ch, bool ok, uint64_t* bar_pub) {
     using S = Smem<W, D, NWG>;
     int* ctl = reinterpret_cast<int*>(sm + S::kOffMisc + 16);
     if (!ok && tid == 0) ctl[1] = 1;
     __syncwarp();
     if (lane == 0) mbar_arrive(&bar_pub[ch.b]);
+  }
+
+  // With one TMEM buffer and W = 64 the epilogue would only wait for the merge warp, and
+  // every pipeline works on chunks of the same slice at once: the epilogue warps merge the
+  // slice's chunk records themselves, several threads per column.
+  __device__ bool epi_merges() const { return !kFoldInMerge<W> && A.nbuf == 1; }
+
+  // Merge the slice's chunk records (from memory) into the merged record of buffer ch.b:
+  // per window row the maximum M and the normaliser Z, and the walk coefficients
+  // gamma_t / (sum gamma * Z_t) of Eq. (4) in rank-1 form.
+  __device__ void merge_records(const Chunk& ch) {
+    using S = Smem<W, D, NWG>;
+    constexpr int kThreads = Roles<NWG>::kEpiThreads;
+    constexpr int P = kThreads / W;            // threads per column (consecutive lanes)
+    static_assert(P >= 1 && P <= 32 && (P & (P - 1)) == 0, "threads per column");
+    const float* rec = A.partial + (long long)ch.slice * A.maxc * A.stride;
+    const int n = ch.nchunks;
+    float* out = reinterpret_cast<float*>(sm + S::kOffMrec) + ch.b * S::kMrec;
+    float* gm = reinterpret_cast<float*>(sm + S::kOffMs);       // [kMaxPairs] merged Gram
+    const int col = tid / P, part = tid % P;
+    {
+      float mx = -INFINITY;
+      for (int r = part; r < n; r += P) mx = fmaxf(mx, rec[(long long)r * A.stride + col]);
+#pragma unroll
+      for (int o = P / 2; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      float z = 0.f;
+      for (int r = part; r < n; r += P) {
+        const float* rr = rec + (long long)r * A.stride;
+        z += rr[W + col] * ex2_approx((rr[col] - mx) * cl2);
+      }
+#pragma unroll
+      for (int o = P / 2; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+      if (part == 0) {
+        out[col] = mx;
+        out[W + col] = z;
+      }
+    }
+    epi_sync<NWG>(bar_id);
+    const int np = H * (H - 1) / 2;
+    // whole warps take part (the shuffles below need every lane); P threads per pair,
+    // lanes past the last pair add nothing
+    if (tid < (np * P + 31) / 32 * 32) {
+      const int k = tid / P;
+      float g = 0.f;
+      int cp = 0, cq = 0;
+      if (k < np) {
+        int u = 0, t = 0;
+        pair_of(k, u, t);
+        cp = W - H + u;
+        cq = W - H + t;
+        const float Mp = out[cp], Mq = out[cq];
+        for (int r = part; r < n; r += P) {
+          const float* rr = rec + (long long)r * A.stride;
+          g += rr[2 * W + k] * ex2_approx(((rr[cp] - Mp) + (rr[cq] - Mq)) * cl2);
+        }
+      }
+#pragma unroll
+      for (int o = P / 2; o > 0; o >>= 1) g += __shfl_xor_sync(0xffffffffu, g, o);
+      if (k < np && part == 0) gm[k] = g / (out[W + cp] * out[W + cq]);   // <P_u, P_t>
+    }
+    epi_sync<NWG>(bar_id);
+    if (tid == 0) {
+      // gamma_t = 1 + sum_{u<t} gamma_u <P_t, P_u>; ||C||_1 = sum_t gamma_t
+      float gam[kMaxWalk], gsum = 0.f;
+      for (int t = 0; t < H; ++t) {
+        float g = 1.f;
+        for (int u = 0; u < t; ++u) g += gam[u] * gm[pair_index(u, t)];
+        gam[t] = g;
+        gsum += g;
+      }
+      for (int t = 0; t < H; ++t) out[2 * W + t] = gam[t] / (gsum * out[W + (W - H + t)]);
+    }
+    epi_sync<NWG>(bar_id);
   }
 
   // Wait for the merge warp's slice statistics, then a, c~, w and the order key of every
@@ -732,24 +816,47 @@ struct Epi {
       posv[r] = (t < ch.ntiles && j < ch.T && (A.out.flags & kEmitKeys))
                     ? __ldg(&c.pos[row_of(c, ch.l, ch.s, ch.h, j)]) : 0;
     }
+    // The random half of each n = 1 reservoir key, ln(u_j), depends on the row's position
+    // and ids only: draw it now, while the merge warp may still be merging the slice.
+    const uint32_t head_id = (uint32_t)((p.layer_id_base + ch.l) * c.kv_heads + ch.h);
+    const uint32_t seq_id = (uint32_t)(p.seq_id_base + ch.s);
+    const bool early_draw = (A.out.flags & kEmitKeys) && p.mode == NX_MODE_RESERVOIR &&
+                            p.n_avg == 1;
+    float lnu[R2];
+#pragma unroll
+    for (int r = 0; r < R2; ++r)
+      lnu[r] = early_draw && wg + NWG * r < ch.ntiles
+                   ? ln_spec(word_to_uniform(draw_block(posv[r], p, head_id, seq_id, 0).x))
+                   : 0.f;
     // the merge warp publishes the slice's merged statistics for this TMEM buffer; thread 0
     // waits (the abort flag may be set by other warps at any time) and everyone acts on
     // its snapshot after the barrier
     uint64_t* bar_mfull = reinterpret_cast<uint64_t*>(sm + S::kOffBar) + 2 * S::kStages + 8;
+    const bool self_merge = epi_merges();
     if (tid == 0) {
-      if (!ctl[1] && !mbar_wait(&bar_mfull[ch.b], ch.use & 1, A.dev_status)) ctl[1] = 1;
+      if (self_merge) {
+        // every chunk record of the slice must be in memory (after a records-only pass
+        // they all are)
+        if (!ctl[1] && A.pass != 2 &&
+            !wait_at_least(&A.arrive[ch.slice], ch.nchunks, A.dev_status))
+          ctl[1] = 1;
+        __threadfence();
+      } else if (!ctl[1] && !mbar_wait(&bar_mfull[ch.b], ch.use & 1, A.dev_status)) {
+        ctl[1] = 1;
+      }
       ctl[2] = ctl[1];
     }
     epi_sync<NWG>(bar_id);
-    if (tid == 0) trace_ev(A, vcta, nev, 5 + 1000 * (ch.slice + 1));
     if (ctl[2]) return false;
+    if (self_merge) merge_records(ch);
+    if (tid == 0) trace_ev(A, vcta, nev, 5 + 1000 * (ch.slice + 1));
     if (!kFoldInMerge<W>) {
       const float* mr = reinterpret_cast<const float*>(sm + S::kOffMrec) + ch.b * S::kMrec;
       const float* m = mc(ch.b);
       if (tid < W) {
         const int w = tid;
         // fold this chunk's max shift into the slice's per-column weights
-        const float shift = exp2f((m[w] - mr[w]) * cl2);
+        const float shift = ex2_approx((m[w] - mr[w]) * cl2);
         ca(ch.b)[w] = shift / ((float)W * mr[W + w]);
         if (w >= W - H) cc(ch.b)[w - (W - H)] = mr[2 * W + (w - (W - H))] * shift;
         if (ch.k == 0 && (A.out.flags & kEmitStats)) {
@@ -770,13 +877,13 @@ struct Epi {
       const float* mcb = mc(ch.b);
       if (lane < CW) {
         const int col = col0 + lane;
-        wc[lane] = ca(ch.b)[col] * exp2f((mwq[col] - mcb[col]) * cl2);
+        wc[lane] = ca(ch.b)[col] * ex2_approx((mwq[col] - mcb[col]) * cl2);
       } else if (lane < CW + kMaxWalk) {
         const int tt = lane - CW;
         float x = 0.f;
         if (tt < H) {
           const int col = W - H + tt;
-          x = cc(ch.b)[tt] * exp2f((mwq[col] - mcb[col]) * cl2);
+          x = cc(ch.b)[tt] * ex2_approx((mwq[col] - mcb[col]) * cl2);
         }
         wc[lane] = x;
       }
@@ -821,9 +928,14 @@ struct Epi {
         }
       }
     }
+    // Pass 2 was the last read of the chunk's TMEM buffer: hand it back to the MMA issuer
+    // now, so that a later chunk's MMAs refill it while the keys are finalized.
+    tc_fence_before();
     epi_sync<NWG>(bar_id);
-    const uint32_t head_id = (uint32_t)((p.layer_id_base + ch.l) * c.kv_heads + ch.h);
-    const uint32_t seq_id = (uint32_t)(p.seq_id_base + ch.s);
+    if (tid == 0) {
+      uint64_t* bar_tempty = reinterpret_cast<uint64_t*>(sm + S::kOffBar) + 2 * S::kStages + 3;
+      mbar_arrive(&bar_tempty[ch.b]);
+    }
     const int bs = p.block_size;
     const int N = units_of(ch.T, bs);
 #pragma unroll
@@ -858,7 +970,8 @@ struct Epi {
       if (A.out.flags & kEmitKeys) {
         uint32_t key = kForcedKey;
         if (!(u < p.n_sink || u >= N - p.n_recent))
-          key = candidate_key(wj, posv[r], p, head_id, seq_id);
+          key = early_draw ? order_key(__fdiv_rn(lnu[r], wj))
+                           : candidate_key(wj, posv[r], p, head_id, seq_id);
         A.out.keys[o] = key;
       }
     }
@@ -877,13 +990,15 @@ struct Epi {
     uint32_t cnt = 0;
     auto finish = [&](const Chunk& ch) -> bool {
       if (tid == 0) trace_ev(A, vcta, nev, 3 + 1000 * (ch.slice + 1));
-      const bool ok = emit<HT>(ch);
+      const bool ok = emit<HT>(ch);   // true: emit handed the buffer back after pass 2
       tc_fence_before();
       epi_sync<NWG>(bar_id);
       if (tid == 0) {
         trace_ev(A, vcta, nev, 4);
-        mbar_arrive(&bar_tempty[ch.b]);
-        if (!ok) ctl[1] = 1;
+        if (!ok) {
+          mbar_arrive(&bar_tempty[ch.b]);
+          ctl[1] = 1;
+        }
       }
       return ok;
     };
@@ -947,6 +1062,7 @@ __device__ void merge_warp(const Args& A, uint8_t* sm, int chunk_rows, int nbuf,
   float* ms = reinterpret_cast<float*>(sm + S::kOffMs);     // [0]: maxima, [1]: normalisers
   uint32_t cnt = 0, htx = 0;
   if (A.pass == 1) return;                 // records only: nothing to merge
+  if (!kFoldInMerge<W> && A.nbuf == 1) return;   // the epilogue merges (Epi::epi_merges)
   Sched sc;
   sched_init(sc, vcta, vgrid);
   int sl, kq, Tq;
@@ -998,9 +1114,9 @@ __device__ void merge_warp(const Args& A, uint8_t* sm, int chunk_rows, int nbuf,
           for (int i = 0; i < n; ++i) mb = fmaxf(mb, stage[i * A.stride + c]);
         Mn[q] = mb;
         if (c < W) {
-          float z = (M[q] == -INFINITY) ? 0.f : Z[q] * exp2f((M[q] - mb) * cl2);
+          float z = (M[q] == -INFINITY) ? 0.f : Z[q] * ex2_approx((M[q] - mb) * cl2);
           for (int i = 0; i < n; ++i)
-            z += stage[i * A.stride + W + c] * exp2f((stage[i * A.stride + c] - mb) * cl2);
+            z += stage[i * A.stride + W + c] * ex2_approx((stage[i * A.stride + c] - mb) * cl2);
           Z[q] = z;
           ms[c] = mb;              // the Gram step needs every column's new maximum
           ms[W + c] = M[q];        // and its previous one
@@ -1009,10 +1125,10 @@ __device__ void merge_warp(const Args& A, uint8_t* sm, int chunk_rows, int nbuf,
       __syncwarp();
       if (gact) {
         const float np = ms[wp], nq = ms[wq], op = ms[W + wp], oq = ms[W + wq];
-        float g = (op == -INFINITY) ? 0.f : G * exp2f(((op - np) + (oq - nq)) * cl2);
+        float g = (op == -INFINITY) ? 0.f : G * ex2_approx(((op - np) + (oq - nq)) * cl2);
         for (int i = 0; i < n; ++i) {
           const float* r = stage + i * A.stride;
-          g += r[2 * W + lane] * exp2f(((r[wp] - np) + (r[wq] - nq)) * cl2);
+          g += r[2 * W + lane] * ex2_approx(((r[wp] - np) + (r[wq] - nq)) * cl2);
         }
         G = g;
       }
@@ -1057,7 +1173,7 @@ __device__ void merge_warp(const Args& A, uint8_t* sm, int chunk_rows, int nbuf,
       for (int q = 0; q < QW; ++q) {
         const int c = lane + 32 * q;
         if (c < W) {
-          const float shift = exp2f((mch[c] - M[q]) * cl2);
+          const float shift = ex2_approx((mch[c] - M[q]) * cl2);
           ca[c] = shift / ((float)W * Z[q]);
           if (c >= W - H) cc[c - (W - H)] = out[2 * W + (c - (W - H))] * shift;
           if (ch.k == 0 && (A.out.flags & kEmitStats)) {
@@ -1072,26 +1188,82 @@ __device__ void merge_warp(const Args& A, uint8_t* sm, int chunk_rows, int nbuf,
   }
 }
 
-// The publisher warp: once the epilogue warps have stored a chunk's record, make it
-// visible device-wide and count it in for its slice (the fence stays off the epilogue's
-// path).
-__device__ void publish_warp(const Args& A, int chunk_rows, int nbuf, uint64_t* bar_pub,
-                             volatile int* abort_flag, int vcta, int vgrid) {
+// The publisher warp: once the epilogue warps have stored a chunk's lane-quarter partials
+// (per-warp column maxima, sums and walk-row Gram sums), it builds the chunk's record
+// (the four quarters rescaled to the chunk maxima, which also go to shared memory for the
+// epilogue and the merge warp), releases the partials' shared memory, makes the record
+// visible device-wide and counts it in for its slice -- all off the epilogue's path.
+template <int W, int D, int NWG>
+__device__ void publish_warp(const Args& A, uint8_t* sm, int chunk_rows, int nbuf, float cl2,
+                             uint64_t* bar_pub, uint64_t* bar_rec, volatile int* abort_flag,
+                             int vcta, int vgrid) {
+  using S = Smem<W, D, NWG>;
+  constexpr int CW = W / NWG;
+  constexpr int RS = S::kRedStride;
+  constexpr int kWalkWg = NWG - 1;
   const int lane = threadIdx.x & 31;
+  const int H = A.p.walk_len;
+  const float* red = reinterpret_cast<const float*>(sm + S::kOffRed);
   Sched sc;
   sched_init(sc, vcta, vgrid);
   int sl, kq, Tq;
   for (uint32_t cnt = 0; sched_next(A, sc, chunk_rows, sl, kq, Tq); ++cnt) {
     const uint32_t b = cnt % nbuf, use = cnt / nbuf;
     int ok = 1;
-    if (lane == 0) {
-      ok = mbar_wait(&bar_pub[b], use & 1, A.dev_status) && !*abort_flag;
-      if (ok) {
-        __threadfence();
-        atomicAdd(&A.arrive[sl], 1);
+    if (lane == 0) ok = mbar_wait(&bar_pub[b], use & 1, A.dev_status) && !*abort_flag;
+    if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+    const float* mwb = reinterpret_cast<const float*>(sm + S::kOffMw) + b * 4 * W;
+    float* m = reinterpret_cast<float*>(sm + S::kOffMc) + b * W;
+    float* rec = A.partial + ((long long)sl * A.maxc + kq) * A.stride;
+    const bool store = A.pass != 2;   // after a records-only pass the records are there
+#pragma unroll
+    for (int q0 = 0; q0 < (W + 31) / 32; ++q0) {
+      const int col = lane + 32 * q0;
+      if (col < W) {
+        const int g = col / CW;
+        float mq[4], mm = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          mq[q] = mwb[q * W + col];
+          mm = fmaxf(mm, mq[q]);
+        }
+        float x = 0.f;                  // quarter sums rescaled to the chunk maximum
+#pragma unroll
+        for (int q = 0; q < 4; ++q) x += red[(4 * g + q) * RS + col] * ex2_approx((mq[q] - mm) * cl2);
+        m[col] = mm;
+        if (store) {
+          rec[col] = mm;                // chunk max (raw)
+          rec[W + col] = x;             // sum relative to it
+        }
       }
     }
-    if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+    if (store && lane < kMaxPairs) {
+      const int k = lane;
+      int u = 0, t = 0;
+      pair_of(k, u, t);
+      float x = 0.f;
+      if (t < H) {
+        const int cp = W - H + u, cq = W - H + t;
+        float mp = -INFINITY, mq = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          mp = fmaxf(mp, mwb[q * W + cp]);
+          mq = fmaxf(mq, mwb[q * W + cq]);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          x += red[(4 * kWalkWg + q) * RS + W + k] *
+               ex2_approx(((mwb[q * W + cp] - mp) + (mwb[q * W + cq] - mq)) * cl2);
+      }
+      rec[2 * W + k] = x;               // Gram entry
+    }
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(bar_rec);             // the partials may be overwritten
+      __threadfence();
+      atomicAdd(&A.arrive[sl], 1);
+    }
+    __syncwarp();
   }
 }
 
@@ -1122,6 +1294,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
   uint64_t* bar_mfull = bar_full + 2 * S::kStages + 8;                 // [3] merged stats ready
   uint64_t* bar_htx = bar_mfull + 3;                                  // merge warp's copies
   uint64_t* bar_pub = bar_htx + 1;                                    // [3] records stored
+  uint64_t* bar_rec = bar_pub + 3;                     // a chunk's partials taken (publisher)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm0 + S::kOffMisc);   // team 0's
   int* ctl = reinterpret_cast<int*>(sm + S::kOffMisc + 16);   // [1] abort, [2-3] snapshots
 
@@ -1149,6 +1322,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
     for (int i = 0; i < 3; ++i) mbar_init(&bar_mfull[i], 1);
     mbar_init(bar_htx, 1);
     for (int i = 0; i < 3; ++i) mbar_init(&bar_pub[i], R::kEpiWarps);
+    mbar_init(bar_rec, 1);
     ctl[0] = 0;
     ctl[1] = 0;
     ctl[2] = 0;
@@ -1175,12 +1349,45 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
   if (warp == R::kProducerWarp) {
     // =================== TMA producer: query images and K tiles ===================
     uint32_t u = 0, qn = 0;
-    int prev_slice = -1;
-    Sched sc;
+    int prev_slice = -1, nev_p = 0;
+    Sched sc, ahead;
     sched_init(sc, vcta, vgrid);
+    sched_init(ahead, vcta, vgrid);
     int slice, k, T;
+    // Every box of a chunk into L2. The shared-memory ring holds only a few tiles, and the
+    // MMAs of a chunk wait for a free TMEM buffer, so the loads stall while the epilogue
+    // works; prefetching the next chunk into L2 keeps HBM streaming meanwhile, and its
+    // loads then come from L2.
+    auto prefetch_chunk = [&](int sl2, int k2, int T2) {
+      int l2, s2, h2;
+      slice_coords(c, sl2, l2, s2, h2);
+      const int j0 = k2 * chunk_rows;
+      const int nt = min(A.tiles_per_chunk, (T2 - j0 + kTileRows - 1) / kTileRows);
+      for (int t = 0; t < nt; ++t) {
+        const int r0 = j0 + t * kTileRows;
+        if (c.page_size == 0) {
+#pragma unroll
+          for (int kb = 0; kb < S::KB; ++kb)
+            tma_prefetch_2d(&tmap, kb * 64, sl2 * c.capacity + r0);
+        } else {
+          const int ps = c.page_size;
+          const int npg = min(kTileRows / ps, (T2 - r0 + ps - 1) / ps);
+          for (int pg = 0; pg < npg; ++pg) {
+            const int page = c.block_table[(long long)s2 * c.max_pages_per_seq + r0 / ps + pg];
+            if (page < 0 || page >= c.num_pages) continue;
+            const int row = (int)((((long long)l2 * c.num_pages + page) * c.kv_heads + h2) * ps);
+            for (int kb = 0; kb < S::KB; ++kb) tma_prefetch_2d(&tmap, kb * 64, row);
+          }
+        }
+      }
+    };
+    int a_sl = 0, a_k = 0, a_T = 0;
+    bool a_ok = sched_next(A, ahead, chunk_rows, a_sl, a_k, a_T);   // = the first chunk
     while (!warp_flag(abort_flag) && sched_next(A, sc, chunk_rows, slice, k, T)) {
       int fail = 0;
+      // keep the lookahead one chunk past this one and bring that chunk into L2
+      if (a_ok) a_ok = sched_next(A, ahead, chunk_rows, a_sl, a_k, a_T);
+      if (lane == 0 && a_ok) prefetch_chunk(a_sl, a_k, a_T);
       if (lane == 0) {
         int l, s, h;
         slice_coords(c, slice, l, s, h);
@@ -1199,6 +1406,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
         for (int t = 0; t < ntiles && !fail; ++t, ++u) {
           const uint32_t st = u % S::kStages, ph = (u / S::kStages) & 1;
           if (!mbar_wait(&bar_empty[st], ph ^ 1, A.dev_status)) { fail = 1; break; }
+          trace_role(A, vcta, 768, nev_p, 40 + t);
           const uint32_t dst = smem_u32(sm + S::kOffK + st * S::kTileBytes);
           const int r0 = j0 + t * kTileRows;
           if (c.page_size == 0) {
@@ -1227,7 +1435,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
   } else if (warp == R::kMmaWarp) {
     // =================== MMA issuer ===================
     uint32_t u = 0, qn = 0, cc = 0;
-    int prev_slice = -1;
+    int prev_slice = -1, nev_m = 0;
     const uint32_t qa = smem_u32(sm + S::kOffQ);
     Sched sc;
     sched_init(sc, vcta, vgrid);
@@ -1238,18 +1446,22 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
         const int j0 = k * chunk_rows;
         const int ntiles = min(A.tiles_per_chunk, (T - j0 + kTileRows - 1) / kTileRows);
         const uint32_t b = cc % nbuf, use = cc / nbuf;
+        trace_role(A, vcta, 512, nev_m, 20);
         // the previous slice's query image may be replaced once its MMAs are done
         if (slice != prev_slice && prev_slice >= 0) mma_commit(bar_qempty);
         if (!mbar_wait(&bar_tempty[b], (use & 1) ^ 1, A.dev_status)) fail = 1;
         tc_fence_after();
+        trace_role(A, vcta, 512, nev_m, 21);
         if (!fail && slice != prev_slice) {
           if (!mbar_wait(bar_qfull, qn & 1, A.dev_status)) fail = 1;
           ++qn;
           prev_slice = slice;
         }
+        trace_role(A, vcta, 512, nev_m, 22);
         for (int t = 0; t < ntiles && !fail; ++t, ++u) {
           const uint32_t st = u % S::kStages, ph = (u / S::kStages) & 1;
           if (!mbar_wait(&bar_full[st], ph, A.dev_status)) { fail = 1; break; }
+          if (t == 0 || t == ntiles - 1) trace_role(A, vcta, 512, nev_m, t == 0 ? 23 : 24);
           tc_fence_after();
           const uint32_t ka = smem_u32(sm + S::kOffK + st * S::kTileBytes);
           const uint32_t dt = tmem + b * buf_cols + (uint32_t)(t * W);
@@ -1268,6 +1480,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
           mma_commit(&bar_empty[st]);      // the stage's smem is free once these finish
         }
         if (!fail) mma_commit(&bar_tfull[b]);   // the chunk's logits are in TMEM buffer b
+        trace_role(A, vcta, 512, nev_m, 25);
         if (fail) *abort_flag = 1;
       }
       if (__shfl_sync(0xffffffffu, fail, 0)) break;
@@ -1278,7 +1491,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
                           abort_flag, vcta, vgrid);
   } else if (warp == R::kPublishWarp) {
     // =================== record publisher ===================
-    publish_warp(A, chunk_rows, nbuf, bar_pub, abort_flag, vcta, vgrid);
+    publish_warp<W, D, NWG>(A, sm, chunk_rows, nbuf, cl2, bar_pub, bar_rec, abort_flag, vcta,
+                            vgrid);
   } else {
     // =================== epilogue: warps [0, 4 NWG) ===================
     Epi<W, D, NWG> epi(A, sm, tmem, buf_cols, cl2, A.p.walk_len, tid, vcta, vgrid, 1 + team);

@@ -132,6 +132,9 @@ class Workload:
     hub_norm: float = 1.0        # hub keys are scaled by this
     n_bridges: int = 0           # bridge slots per slice
     query_gain: float = 8.0      # gain of the hub direction in a window query
+    query_run: int = 1           # window rows come in runs of this many rows on one pair
+                                 # of adjacent hubs (alternating between the two), so
+                                 # consecutive rows co-attend the pair's bridges
     zipf: float = 0.0            # > 0: hub rank of a query ~ Zipf(zipf)
     n_topics: int = 0
     lognormal_sigma: float = 0.0
@@ -375,6 +378,12 @@ def query_rows(wl: Workload, sid: int, step: int) -> np.ndarray:
         target = rng.choice(hubs.size, size=W, p=p)
     else:
         target = rng.integers(0, hubs.size, size=W)
+    if wl.query_run > 1:
+        # runs of rows on one adjacent hub pair (i, i + 1), alternating between the two
+        for r0 in range(0, W, wl.query_run):
+            i = int(rng.integers(0, hubs.size))
+            for r in range(r0, min(W, r0 + wl.query_run)):
+                target[r] = (i + (r - r0) % 2) % hubs.size
     q = noise + wl.query_gain * unit[target][None, :, :]
     return q.astype(np.float32)
 
