@@ -284,6 +284,10 @@ nx_status nexus_evict_step(nx_cache* cache, const void* q, const nx_params* para
   out.keys = keys;
   out.flags = kEmitKeys;
   NX_TRY(run_scores(*cache, q, *params, L, w, out, dev_status, st, &launches));
+  // n > 1: the scorers left w in the key array; the n-averaged keys replace it in place
+  if (params->n_avg > 1)
+    NX_TRY(launch_keys_from_w(*cache, *params, reinterpret_cast<const float*>(keys), keys,
+                              newlen, st, &launches));
   NX_TRY(launch_select(*cache, keys, keep, newlen, params->block_size, st, &launches));
   NX_TRY(launch_compact(*cache, *params, L, w, keep, newlen, dev_status, st, &launches));
   return finish(cudaSuccess, launches);

@@ -226,6 +226,15 @@ static __device__ __noinline__ float averaged_key(float w, int32_t pos, const nx
   return __fadd_rn(__fmul_rn(M, r), ln_spec(S));
 }
 
+// Order key of one candidate unit at n = 1 (§2.3, Eq. (6)): ln(u)/w for the reservoir
+// (Efraimidis-Spirakis), w itself for the top-K template.
+__device__ __forceinline__ uint32_t candidate_key1(float w, int32_t pos, const nx_params& p,
+                                                   uint32_t head_id, uint32_t seq_id) {
+  if (p.mode == NX_MODE_TOPK) return order_key(w);
+  const uint4 r = draw_block(pos, p, head_id, seq_id, 0);
+  return order_key(__fdiv_rn(ln_spec(word_to_uniform(r.x)), w));
+}
+
 // Order key of one candidate unit (§2.3, Eq. (6)): ln(u)/w for the reservoir at n = 1
 // (Efraimidis-Spirakis), the log of the n-averaged priority for n > 1, w itself for the
 // top-K template.

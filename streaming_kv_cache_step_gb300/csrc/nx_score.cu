@@ -343,9 +343,11 @@ score_simt_kernel(nx_cache c, nx_params p, const float* __restrict__ qbar,
   if (out.flags & kEmitW) out.w[o] = wj;
   if (out.flags & kEmitKeys) {
     uint32_t key = kForcedKey;
-    if (!(u < p.n_sink || u >= N - p.n_recent)) {
+    if (p.n_avg > 1) {
+      key = __float_as_uint(wj);   // the averaged keys are drawn by a pass of their own
+    } else if (!(u < p.n_sink || u >= N - p.n_recent)) {
       const uint32_t head_id = (uint32_t)((p.layer_id_base + l) * c.kv_heads + h);
-      key = candidate_key(wj, c.pos[r], p, head_id, (uint32_t)(p.seq_id_base + s));
+      key = candidate_key1(wj, c.pos[r], p, head_id, (uint32_t)(p.seq_id_base + s));
     }
     out.keys[o] = key;
   }

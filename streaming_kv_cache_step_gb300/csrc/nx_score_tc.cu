@@ -133,15 +133,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// L2 prefetch of one tensor-map box (no shared memory, no barrier): the bytes are in L2
-// when the load of the same box is issued later.
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y)
-               : "memory");
-}
-
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
                                           uint64_t* bar) {
   asm volatile(
@@ -382,8 +373,6 @@ struct Sched {
   uint32_t mask;     // lanes whose slice has a chunk left for this CTA
   int k, T, n;       // this lane's slice: the next chunk index for this CTA, its length,
                      // its chunk count
-  int pre_nl, pre_t; // the next batch's new length and length for this lane (loaded one
-                     // batch ahead, so that a refill does not wait on global memory)
 };
 
 __device__ __forceinline__ void sched_init(Sched& S, int cta, int ncta) {
@@ -395,8 +384,6 @@ __device__ __forceinline__ void sched_init(Sched& S, int cta, int ncta) {
   S.k = 0;
   S.T = 0;
   S.n = 0;
-  S.pre_nl = -2;     // nothing loaded ahead yet
-  S.pre_t = 0;
 }
 
 // Warp-collective: the next chunk of this CTA; false once there is none.
@@ -408,17 +395,9 @@ __device__ __forceinline__ bool sched_next(const Args& A, Sched& S, int chunk_ro
     if (S.base >= A.slices) return false;
     const int sl = S.base + lane;
     int nl = -1, t = 0, n = 0;
-    if (S.pre_nl != -2) {
-      nl = S.pre_nl;
-      t = S.pre_t;
-    } else if (sl < A.slices) {
+    if (sl < A.slices) {
       nl = __ldg(&A.newlen[sl]);
       t = __ldg(&A.c.lens[sl]);
-    }
-    {
-      const int sl2 = sl + 32;        // load the next batch now; used at the next refill
-      S.pre_nl = sl2 < A.slices ? __ldg(&A.newlen[sl2]) : -1;
-      S.pre_t = sl2 < A.slices ? __ldg(&A.c.lens[sl2]) : 0;
     }
     if (sl < A.slices && nl >= 0) n = (t + chunk_rows - 1) / chunk_rows;
     else t = 0;
@@ -816,18 +795,8 @@ struct Epi {
       posv[r] = (t < ch.ntiles && j < ch.T && (A.out.flags & kEmitKeys))
                     ? __ldg(&c.pos[row_of(c, ch.l, ch.s, ch.h, j)]) : 0;
     }
-    // The random half of each n = 1 reservoir key, ln(u_j), depends on the row's position
-    // and ids only: draw it now, while the merge warp may still be merging the slice.
     const uint32_t head_id = (uint32_t)((p.layer_id_base + ch.l) * c.kv_heads + ch.h);
     const uint32_t seq_id = (uint32_t)(p.seq_id_base + ch.s);
-    const bool early_draw = (A.out.flags & kEmitKeys) && p.mode == NX_MODE_RESERVOIR &&
-                            p.n_avg == 1;
-    float lnu[R2];
-#pragma unroll
-    for (int r = 0; r < R2; ++r)
-      lnu[r] = early_draw && wg + NWG * r < ch.ntiles
-                   ? ln_spec(word_to_uniform(draw_block(posv[r], p, head_id, seq_id, 0).x))
-                   : 0.f;
     // the merge warp publishes the slice's merged statistics for this TMEM buffer; thread 0
     // waits (the abort flag may be set by other warps at any time) and everyone acts on
     // its snapshot after the barrier
@@ -969,9 +938,10 @@ struct Epi {
       if (A.out.flags & kEmitW) A.out.w[o] = wj;
       if (A.out.flags & kEmitKeys) {
         uint32_t key = kForcedKey;
-        if (!(u < p.n_sink || u >= N - p.n_recent))
-          key = early_draw ? order_key(__fdiv_rn(lnu[r], wj))
-                           : candidate_key(wj, posv[r], p, head_id, seq_id);
+        if (p.n_avg > 1)
+          key = __float_as_uint(wj);   // the averaged keys are drawn by a pass of their own
+        else if (!(u < p.n_sink || u >= N - p.n_recent))
+          key = candidate_key1(wj, posv[r], p, head_id, seq_id);
         A.out.keys[o] = key;
       }
     }
@@ -1350,44 +1320,11 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
     // =================== TMA producer: query images and K tiles ===================
     uint32_t u = 0, qn = 0;
     int prev_slice = -1, nev_p = 0;
-    Sched sc, ahead;
+    Sched sc;
     sched_init(sc, vcta, vgrid);
-    sched_init(ahead, vcta, vgrid);
     int slice, k, T;
-    // Every box of a chunk into L2. The shared-memory ring holds only a few tiles, and the
-    // MMAs of a chunk wait for a free TMEM buffer, so the loads stall while the epilogue
-    // works; prefetching the next chunk into L2 keeps HBM streaming meanwhile, and its
-    // loads then come from L2.
-    auto prefetch_chunk = [&](int sl2, int k2, int T2) {
-      int l2, s2, h2;
-      slice_coords(c, sl2, l2, s2, h2);
-      const int j0 = k2 * chunk_rows;
-      const int nt = min(A.tiles_per_chunk, (T2 - j0 + kTileRows - 1) / kTileRows);
-      for (int t = 0; t < nt; ++t) {
-        const int r0 = j0 + t * kTileRows;
-        if (c.page_size == 0) {
-#pragma unroll
-          for (int kb = 0; kb < S::KB; ++kb)
-            tma_prefetch_2d(&tmap, kb * 64, sl2 * c.capacity + r0);
-        } else {
-          const int ps = c.page_size;
-          const int npg = min(kTileRows / ps, (T2 - r0 + ps - 1) / ps);
-          for (int pg = 0; pg < npg; ++pg) {
-            const int page = c.block_table[(long long)s2 * c.max_pages_per_seq + r0 / ps + pg];
-            if (page < 0 || page >= c.num_pages) continue;
-            const int row = (int)((((long long)l2 * c.num_pages + page) * c.kv_heads + h2) * ps);
-            for (int kb = 0; kb < S::KB; ++kb) tma_prefetch_2d(&tmap, kb * 64, row);
-          }
-        }
-      }
-    };
-    int a_sl = 0, a_k = 0, a_T = 0;
-    bool a_ok = sched_next(A, ahead, chunk_rows, a_sl, a_k, a_T);   // = the first chunk
     while (!warp_flag(abort_flag) && sched_next(A, sc, chunk_rows, slice, k, T)) {
       int fail = 0;
-      // keep the lookahead one chunk past this one and bring that chunk into L2
-      if (a_ok) a_ok = sched_next(A, ahead, chunk_rows, a_sl, a_k, a_T);
-      if (lane == 0 && a_ok) prefetch_chunk(a_sl, a_k, a_T);
       if (lane == 0) {
         int l, s, h;
         slice_coords(c, slice, l, s, h);

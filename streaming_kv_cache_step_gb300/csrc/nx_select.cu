@@ -17,9 +17,10 @@ namespace {
 constexpr int kSelThreads = 1024;
 
 // Order key of every unit of every slice from caller-given weights (one thread per unit;
-// a unit's Philox position is that of its first row).
-__global__ void keys_from_w_kernel(nx_cache c, nx_params p, const float* __restrict__ w,
-                                   uint32_t* __restrict__ keys, const int32_t* __restrict__ newlen) {
+// a unit's Philox position is that of its first row). w may alias keys (each thread reads
+// its unit's weight before writing its key).
+__global__ void keys_from_w_kernel(nx_cache c, nx_params p, const float* w, uint32_t* keys,
+                                   const int32_t* __restrict__ newlen) {
   const int slice = blockIdx.x;
   if (newlen[slice] < 0) return;
   const int N = units_of(c.lens[slice], p.block_size);
