@@ -20,10 +20,6 @@ namespace nx {
 namespace {
 
 constexpr int kCompactThreads = 256;
-#ifndef NX_COMPACT_BUFS
-#define NX_COMPACT_BUFS 2
-#endif
-constexpr int kCompactBufs = NX_COMPACT_BUFS;   // tiles staged per block (>= 2)
 
 __device__ __forceinline__ bool slice_ok(const nx_cache& c, const nx_params& p, int slice,
                                          int32_t* dev_status) {
@@ -77,11 +73,6 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
-// Wait until at most N of this thread's cp.async groups are still in flight.
-template <int N>
-__device__ __forceinline__ void cp_async_wait_pending() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
@@ -93,8 +84,8 @@ struct TileSlot {
   int moves;        // any row with keep[i] != i
 };
 
-// kCompactBufs shared-memory buffers: while tile c's rows are written from one, the
-// sources of the next kCompactBufs - 1 tiles stream into the others with cp.async.
+// Two shared-memory buffers: while tile c's rows are written from one, tile c+1's sources
+// stream into the other with cp.async.
 __global__ void __launch_bounds__(kCompactThreads)
 compact_kernel(nx_cache c, const int32_t* __restrict__ keep, const int32_t* __restrict__ newlen,
                int* tile_flags, unsigned long long* work, int tiles_per_slice,
@@ -104,11 +95,11 @@ compact_kernel(nx_cache c, const int32_t* __restrict__ keep, const int32_t* __re
   const int chunks = row_bytes / 16;                    // 16-byte pieces per row
   const int per_buf = 2 * kCompactRows * chunks;        // K then V
   uint4* bufs = reinterpret_cast<uint4*>(smem);
-  __shared__ int s_src[kCompactBufs][kCompactRows];
-  __shared__ int s_pos[kCompactBufs][kCompactRows];
-  __shared__ long long s_srow[kCompactBufs][kCompactRows];   // source / destination rows
-  __shared__ long long s_drow[kCompactBufs][kCompactRows];
-  __shared__ TileSlot s_slot[kCompactBufs];
+  __shared__ int s_src[2][kCompactRows];
+  __shared__ int s_pos[2][kCompactRows];
+  __shared__ long long s_srow[2][kCompactRows];   // source and destination row indices
+  __shared__ long long s_drow[2][kCompactRows];
+  __shared__ TileSlot s_slot[2];
   __shared__ long long s_claim;
   __shared__ int s_ok;
   grid_dep_wait();                 // kept slots and new lengths come from the kernels before
@@ -182,14 +173,12 @@ compact_kernel(nx_cache c, const int32_t* __restrict__ keep, const int32_t* __re
   };
 
   int b = 0;
-#pragma unroll 1
-  for (int i = 0; i < kCompactBufs - 1; ++i) stage(i);
+  stage(b);
   for (;;) {
     const TileSlot cur = s_slot[b];
     if (cur.tile >= total_tiles) break;
-    // the current tile's reads are complete (only the later tiles' groups may still be in
-    // flight): publish "read done"
-    cp_async_wait_pending<kCompactBufs - 2>();
+    // the current tile's reads are complete: publish "read done"
+    cp_async_wait_all();
     __syncthreads();
     if (threadIdx.x == 0) {
       // the release store orders the block's completed reads (barrier above) before the
@@ -198,9 +187,8 @@ compact_kernel(nx_cache c, const int32_t* __restrict__ keep, const int32_t* __re
       if (cur.t == 0 && cur.tile < total_tiles && cur.nl >= 0) c.lens[cur.slice] = cur.nl;
       s_ok = 1;
     }
-    // start the reads of the tile kCompactBufs - 1 ahead, into the buffer the previous
-    // tile was written from; they proceed while this tile waits and writes
-    stage((b + kCompactBufs - 1) % kCompactBufs);
+    // start the next tile's reads; they proceed while this tile waits and writes
+    stage(b ^ 1);
     if (cur.moves) {
       // every earlier tile of the slice has read its sources (only those can read rows
       // [i0, i0 + n); none of them waits before publishing)
@@ -224,7 +212,7 @@ compact_kernel(nx_cache c, const int32_t* __restrict__ keep, const int32_t* __re
       }
     }
     __syncthreads();
-    b = (b + 1) % kCompactBufs;
+    b ^= 1;
   }
   cp_async_wait_all();
 }
@@ -243,7 +231,7 @@ cudaError_t launch_compact(const nx_cache& c, const nx_params& p, const WsLayout
                            const int32_t* keep, const int32_t* newlen, int32_t* dev_status,
                            cudaStream_t st, int* launches, long long skip_signal_tile) {
   const int row_bytes = c.head_dim * (c.dtype == NX_DTYPE_BF16 ? 2 : 4);
-  const size_t smem = kCompactBufs * 2 * (size_t)kCompactRows * row_bytes;   // K + V buffers
+  const size_t smem = 2 * 2 * (size_t)kCompactRows * row_bytes;   // two buffers of K + V
   int dev = 0, sms = 0, per_sm = 0;
   cudaGetDevice(&dev);
   // the tile bookkeeping lives in static shared memory: the opt-in is needed as soon as

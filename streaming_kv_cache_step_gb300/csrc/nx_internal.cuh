@@ -197,31 +197,46 @@ __device__ __forceinline__ float log_draw(int32_t pos, const nx_params& p, uint3
 
 // §2.3 Eq. (6) for n > 1, in the log domain: with l_i = ln(u_i), M = max_i l_i and
 // r = 1/w, key = M r + ln(sum_{i < n} exp((l_i - M) r)) = ln(n pi_j); -inf for w = 0.
-// Up to 8 draws stay in registers; more are drawn twice (same values both times).
-static __device__ __noinline__ float averaged_key(float w, int32_t pos, const nx_params& p,
-                                           uint32_t head_id, uint32_t seq_id) {
-  const int n = p.n_avg;
-  float l8[8];
-  float M = -__int_as_float(0x7F800000);
-  uint4 blk = make_uint4(0, 0, 0, 0);
-  for (int i = 0; i < n; ++i) {
-    if ((i & 3) == 0) blk = draw_block(pos, p, head_id, seq_id, (uint32_t)i >> 2);
-    const float l = ln_spec(word_to_uniform(word_of(blk, i & 3)));
-    if (i < 8) l8[i] = l;
-    M = fmaxf(M, l);
-  }
+// NT > 0: n = NT draws, unrolled and kept in registers. NT = 0: n = p.n_avg draws, taken
+// twice (the same values both times) so that nothing is indexed at run time. The sum runs
+// over i = 0, 1, ..., n - 1 in that order either way, so both give the same bits.
+template <int NT>
+__device__ __forceinline__ float averaged_key(float w, int32_t pos, const nx_params& p,
+                                              uint32_t head_id, uint32_t seq_id) {
   const float r = __fdiv_rn(1.0f, w);
   if (!(r < __int_as_float(0x7F800000))) return -__int_as_float(0x7F800000);
+  float M = -__int_as_float(0x7F800000);
   float S = 0.0f;
-  for (int i = 0; i < n; ++i) {
-    float l;
-    if (n <= 8) {
-      l = l8[i];
-    } else {
-      if ((i & 3) == 0) blk = draw_block(pos, p, head_id, seq_id, (uint32_t)i >> 2);
-      l = ln_spec(word_to_uniform(word_of(blk, i & 3)));
+  if constexpr (NT > 0) {
+    float l[NT];
+#pragma unroll
+    for (int g = 0; g < (NT + 3) / 4; ++g) {
+      const uint4 blk = draw_block(pos, p, head_id, seq_id, (uint32_t)g);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (4 * g + i < NT) l[4 * g + i] = ln_spec(word_to_uniform(word_of(blk, i)));
     }
-    S = __fadd_rn(S, exp_spec(__fmul_rn(__fsub_rn(l, M), r)));
+#pragma unroll
+    for (int i = 0; i < NT; ++i) M = fmaxf(M, l[i]);
+#pragma unroll
+    for (int i = 0; i < NT; ++i) S = __fadd_rn(S, exp_spec(__fmul_rn(__fsub_rn(l[i], M), r)));
+  } else {
+    const int n = p.n_avg;
+    for (int g = 0; 4 * g < n; ++g) {
+      const uint4 blk = draw_block(pos, p, head_id, seq_id, (uint32_t)g);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (4 * g + i < n) M = fmaxf(M, ln_spec(word_to_uniform(word_of(blk, i))));
+    }
+    for (int g = 0; 4 * g < n; ++g) {
+      const uint4 blk = draw_block(pos, p, head_id, seq_id, (uint32_t)g);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (4 * g + i < n) {
+          const float l = ln_spec(word_to_uniform(word_of(blk, i)));
+          S = __fadd_rn(S, exp_spec(__fmul_rn(__fsub_rn(l, M), r)));
+        }
+    }
   }
   return __fadd_rn(__fmul_rn(M, r), ln_spec(S));
 }
@@ -235,15 +250,17 @@ __device__ __forceinline__ uint32_t candidate_key1(float w, int32_t pos, const n
   return order_key(__fdiv_rn(ln_spec(word_to_uniform(r.x)), w));
 }
 
-// Order key of one candidate unit (§2.3, Eq. (6)): ln(u)/w for the reservoir at n = 1
-// (Efraimidis-Spirakis), the log of the n-averaged priority for n > 1, w itself for the
-// top-K template.
+// Order key of one candidate unit (§2.3, Eq. (6)) with NT draws known at compile time
+// (NT = 1: ln(u)/w, Efraimidis-Spirakis; 0: p.n_avg draws), w itself for the top-K template.
+template <int NT>
 __device__ __forceinline__ uint32_t candidate_key(float w, int32_t pos, const nx_params& p,
                                                   uint32_t head_id, uint32_t seq_id) {
-  if (p.mode == NX_MODE_TOPK) return order_key(w);
-  if (p.n_avg > 1) return order_key(averaged_key(w, pos, p, head_id, seq_id));
-  const uint4 r = draw_block(pos, p, head_id, seq_id, 0);
-  return order_key(__fdiv_rn(ln_spec(word_to_uniform(r.x)), w));
+  if constexpr (NT == 1) {
+    return candidate_key1(w, pos, p, head_id, seq_id);
+  } else {
+    if (p.mode == NX_MODE_TOPK) return order_key(w);
+    return order_key(averaged_key<NT>(w, pos, p, head_id, seq_id));
+  }
 }
 
 // The budget (units kept) of a slice: its own when the caller gives per-slice budgets.

@@ -19,6 +19,7 @@ constexpr int kSelThreads = 1024;
 // Order key of every unit of every slice from caller-given weights (one thread per unit;
 // a unit's Philox position is that of its first row). w may alias keys (each thread reads
 // its unit's weight before writing its key).
+template <int NT>
 __global__ void keys_from_w_kernel(nx_cache c, nx_params p, const float* w, uint32_t* keys,
                                    const int32_t* __restrict__ newlen) {
   const int slice = blockIdx.x;
@@ -32,8 +33,8 @@ __global__ void keys_from_w_kernel(nx_cache c, nx_params p, const float* w, uint
   uint32_t key = kForcedKey;
   if (!(u < p.n_sink || u >= N - p.n_recent)) {
     const uint32_t head_id = (uint32_t)((p.layer_id_base + l) * c.kv_heads + h);
-    key = candidate_key(w[o], c.pos[row_of(c, l, s, h, u * p.block_size)], p, head_id,
-                        (uint32_t)(p.seq_id_base + s));
+    key = candidate_key<NT>(w[o], c.pos[row_of(c, l, s, h, u * p.block_size)], p, head_id,
+                            (uint32_t)(p.seq_id_base + s));
   }
   keys[o] = key;
 }
@@ -256,7 +257,18 @@ cudaError_t launch_keys_from_w(const nx_cache& c, const nx_params& p, const floa
                                int* launches) {
   const long long slices = (long long)c.layers * c.seqs * c.kv_heads;
   dim3 grid((unsigned)slices, (c.capacity + 255) / 256);
-  keys_from_w_kernel<<<grid, 256, 0, st>>>(c, p, w, keys, newlen);
+  // the usual draw counts unrolled with their draws in registers; the rest drawn twice
+  switch (p.n_avg) {
+    case 1: keys_from_w_kernel<1><<<grid, 256, 0, st>>>(c, p, w, keys, newlen); break;
+    case 2: keys_from_w_kernel<2><<<grid, 256, 0, st>>>(c, p, w, keys, newlen); break;
+    case 3: keys_from_w_kernel<3><<<grid, 256, 0, st>>>(c, p, w, keys, newlen); break;
+    case 4: keys_from_w_kernel<4><<<grid, 256, 0, st>>>(c, p, w, keys, newlen); break;
+    case 5: keys_from_w_kernel<5><<<grid, 256, 0, st>>>(c, p, w, keys, newlen); break;
+    case 6: keys_from_w_kernel<6><<<grid, 256, 0, st>>>(c, p, w, keys, newlen); break;
+    case 7: keys_from_w_kernel<7><<<grid, 256, 0, st>>>(c, p, w, keys, newlen); break;
+    case 8: keys_from_w_kernel<8><<<grid, 256, 0, st>>>(c, p, w, keys, newlen); break;
+    default: keys_from_w_kernel<0><<<grid, 256, 0, st>>>(c, p, w, keys, newlen); break;
+  }
   note_launch(st, launches, "keys_from_w");
   return cudaGetLastError();
 }
