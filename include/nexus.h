@@ -263,6 +263,16 @@ nx_status nexus_debug_compact(nx_cache* cache, const int32_t* keep_idx, const nx
 void nexus_debug_force_simt(int32_t on);
 
 /*
+ * Testing hook: which kernel the compaction takes, process-wide. 1: the tile kernel
+ * (32-row destination tiles claimed in order by persistent blocks, each waiting until the
+ * earlier tiles of its slice have read their sources); 2: one warp per slice, its rows in
+ * order through registers (rows of 128, 256 or 512 bytes); any other value: the automatic
+ * choice (a warp per slice when there are at least eight slices per SM and the row size
+ * allows). nexus_debug_compact always takes the tile kernel.
+ */
+void nexus_debug_compact_kernel(int32_t which);
+
+/*
  * Testing hook: the tensor-core scorer's layout, process-wide. teams = 2 asks for two
  * independent pipelines per CTA (256 TMEM columns and eight epilogue warps each), 1 for
  * one pipeline per CTA (512 columns, sixteen epilogue warps), any other value for the

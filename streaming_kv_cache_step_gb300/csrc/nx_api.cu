@@ -331,6 +331,8 @@ int32_t nexus_last_scorer(void) { return g_last_scorer; }
 
 void nexus_debug_force_simt(int32_t on) { g_force_simt.store(on != 0); }
 
+void nexus_debug_compact_kernel(int32_t which) { nx::compact_set_kernel(which); }
+
 void nexus_debug_scorer_layout(int32_t teams) {
   nx::tc_set_layout(teams == 1 || teams == 2 ? teams : 0);
 }

@@ -14,6 +14,8 @@
 // without waiting, or its next one, published once the current tile -- which only waits
 // on lower, hence published, tiles -- is written. Rows with keep[i] == i are neither
 // read nor written.
+#include <atomic>
+
 #include "nx_internal.cuh"
 
 namespace nx {
@@ -217,6 +219,107 @@ compact_kernel(nx_cache c, const int32_t* __restrict__ keep, const int32_t* __re
   cp_async_wait_all();
 }
 
+
+// Caches with many slices: one warp per slice, its destination rows in increasing order,
+// with no flags and no shared memory. The warp takes 32 destinations at a time (their
+// kept units read once, the next 32's read meanwhile) and moves their K and V rows through
+// registers in batches of 2 KB per tensor, the next batch's loads in flight while this
+// one is written. Nothing else needs ordering: a batch reads rows at or after its own
+// destinations, which lie after every earlier batch's destinations, so a write never
+// destroys a row that a later read of the slice still needs. CH = 16-byte pieces per row.
+__device__ __forceinline__ int src_row_of(const int32_t* kp, int i, int bs) {
+  return bs == 1 ? kp[i] : kp[i / bs] * bs + i % bs;
+}
+
+template <int CH>
+__device__ __forceinline__ void slice_batch_load(const uint4* K, const uint4* V, long long srow,
+                                                 long long drow, int b, int lane, uint4* k,
+                                                 uint4* v, long long* d) {
+  constexpr int RPL = 32 / CH;                     // rows per warp-wide 16-byte load
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int rr = b * 4 * RPL + q * RPL + lane / CH;   // this lane's row of the group
+    const long long sr = __shfl_sync(0xffffffffu, srow, rr);
+    d[q] = __shfl_sync(0xffffffffu, drow, rr);
+    if (d[q] >= 0) {
+      k[q] = K[sr * CH + lane % CH];
+      v[q] = V[sr * CH + lane % CH];
+    }
+  }
+}
+
+template <int CH>
+__device__ __forceinline__ void slice_batch_store(uint4* K, uint4* V, int lane, const uint4* k,
+                                                  const uint4* v, const long long* d) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (d[q] >= 0) {
+      K[d[q] * CH + lane % CH] = k[q];
+      V[d[q] * CH + lane % CH] = v[q];
+    }
+  }
+}
+
+template <int CH>
+__global__ void __launch_bounds__(kCompactThreads)
+compact_slices_kernel(nx_cache c, const int32_t* __restrict__ keep,
+                      const int32_t* __restrict__ newlen, long long slices, int bs) {
+  constexpr int NB = 32 / (4 * (32 / CH));   // batches per group of 32 destination rows
+  grid_dep_wait();                 // kept slots and new lengths come from the kernels before
+  const int lane = threadIdx.x & 31;
+  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+  uint4* K = reinterpret_cast<uint4*>(c.k);
+  uint4* V = reinterpret_cast<uint4*>(c.v);
+  for (long long sl = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; sl < slices;
+       sl += nwarps) {
+    const int nl = newlen[sl];
+    if (nl < 0) continue;
+    int l, s, h;
+    slice_coords(c, (int)sl, l, s, h);
+    const int32_t* kp = keep + sl * (long long)c.capacity;
+    int srcn = lane < nl ? src_row_of(kp, lane, bs) : 0;
+    for (int g0 = 0; g0 < nl; g0 += 32) {
+      const int i = g0 + lane;
+      const int src = srcn;
+      srcn = i + 32 < nl ? src_row_of(kp, i + 32, bs) : 0;   // the next group's sources
+      const bool mv = i < nl && src != i;
+      const long long srow = mv ? row_of(c, l, s, h, src) : -1;
+      const long long drow = mv ? row_of(c, l, s, h, i) : -1;
+      const int pv = mv ? c.pos[srow] : 0;
+      if (__ballot_sync(0xffffffffu, mv) == 0) continue;   // nothing of this group moves
+      uint4 ka[4], va[4], kb[4], vb[4];
+      long long da[4], db[4];
+      slice_batch_load<CH>(K, V, srow, drow, 0, lane, ka, va, da);
+#pragma unroll
+      for (int b = 0; b < NB; b += 2) {
+        if (b + 1 < NB) slice_batch_load<CH>(K, V, srow, drow, b + 1, lane, kb, vb, db);
+        slice_batch_store<CH>(K, V, lane, ka, va, da);
+        if (b + 2 < NB) slice_batch_load<CH>(K, V, srow, drow, b + 2, lane, ka, va, da);
+        if (b + 1 < NB) slice_batch_store<CH>(K, V, lane, kb, vb, db);
+      }
+      if (mv) c.pos[drow] = pv;
+    }
+    if (lane == 0) c.lens[sl] = nl;
+  }
+}
+
+std::atomic<int> g_compact_kernel{0};   // 0: automatic, 1: tiles, 2: one warp per slice
+
+template <int CH>
+cudaError_t launch_slices(const nx_cache& c, const int32_t* keep, const int32_t* newlen,
+                          long long slices, int bs, int sms, cudaStream_t st) {
+  int per_sm = 0;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, compact_slices_kernel<CH>,
+                                                kCompactThreads, 0);
+  constexpr int kWarps = kCompactThreads / 32;
+  long long grid = (long long)sms * (per_sm > 0 ? per_sm : 1);
+  const long long need = (slices + kWarps - 1) / kWarps;
+  if (grid > need) grid = need;
+  if (grid < 1) grid = 1;
+  return launch_after(compact_slices_kernel<CH>, dim3((unsigned)grid), dim3(kCompactThreads),
+                      0, st, c, keep, newlen, slices, bs);
+}
+
 }  // namespace
 
 cudaError_t launch_newlen(const nx_cache& c, const nx_params& p, int32_t* newlen,
@@ -234,6 +337,24 @@ cudaError_t launch_compact(const nx_cache& c, const nx_params& p, const WsLayout
   const size_t smem = 2 * 2 * (size_t)kCompactRows * row_bytes;   // two buffers of K + V
   int dev = 0, sms = 0, per_sm = 0;
   cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // Many slices (at least eight per SM): one warp per slice, no cross-block ordering.
+  // Otherwise (and for the failure-detection hook) the tile kernel, which spreads a
+  // slice over many blocks.
+  const int which = g_compact_kernel.load(std::memory_order_relaxed);
+  const int ch = row_bytes / 16;
+  const bool fits = row_bytes % 16 == 0 && (ch == 8 || ch == 16 || ch == 32);
+  if (skip_signal_tile < 0 && fits &&
+      (which == 2 || (which == 0 && L.slices >= 8LL * (sms > 0 ? sms : 1)))) {
+    const int32_t* nlp = newlen;
+    const cudaError_t e =
+        ch == 8 ? launch_slices<8>(c, keep, nlp, L.slices, p.block_size, sms, st)
+        : ch == 16 ? launch_slices<16>(c, keep, nlp, L.slices, p.block_size, sms, st)
+                   : launch_slices<32>(c, keep, nlp, L.slices, p.block_size, sms, st);
+    if (e != cudaSuccess) return e;
+    note_launch(st, launches, "compact_slices");
+    return cudaGetLastError();
+  }
   // the tile bookkeeping lives in static shared memory: the opt-in is needed as soon as
   // static + dynamic bytes pass the 48 KB default
   static const size_t static_bytes = [] {
@@ -246,7 +367,6 @@ cudaError_t launch_compact(const nx_cache& c, const nx_params& p, const WsLayout
         compact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, compact_kernel, kCompactThreads, smem);
   const long long total = L.slices * L.tiles_per_slice;
   long long grid = (long long)sms * (per_sm > 0 ? per_sm : 1);
@@ -260,5 +380,7 @@ cudaError_t launch_compact(const nx_cache& c, const nx_params& p, const WsLayout
   note_launch(st, launches, "compact");
   return cudaGetLastError();
 }
+
+void compact_set_kernel(int which) { g_compact_kernel.store(which == 1 || which == 2 ? which : 0); }
 
 }  // namespace nx

@@ -378,5 +378,7 @@ cudaError_t launch_newlen(const nx_cache& c, const nx_params& p, int32_t* newlen
 cudaError_t launch_compact(const nx_cache& c, const nx_params& p, const WsLayout& L, char* ws,
                            const int32_t* keep, const int32_t* newlen, int32_t* dev_status,
                            cudaStream_t st, int* launches, long long skip_signal_tile = -1);
+// which compaction kernel launch_compact() takes: 0 automatic, 1 tiles, 2 a warp per slice
+void compact_set_kernel(int which);
 
 }  // namespace nx

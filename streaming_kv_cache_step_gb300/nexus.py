@@ -29,7 +29,7 @@ SYMBOLS = ("nexus_workspace_bytes", "nexus_direct_scores", "nexus_walk",
            "nexus_last_launch_count", "nexus_debug_compact", "nexus_last_launch_name",
            "nexus_profile_next_call", "nexus_debug_force_simt", "nexus_debug_set_trace",
            "nexus_debug_scorer_config", "nexus_debug_scorer_layout", "kv_compact_noalloc",
-           "nexus_last_scorer")
+           "nexus_last_scorer", "nexus_debug_compact_kernel")
 SCORER_NONE, SCORER_TENSOR_CORE, SCORER_CUDA_CORE, SCORER_TENSOR_CORE_TWO_PASS = 0, 1, 2, 3
 
 
@@ -95,6 +95,8 @@ def load(path: str = LIB_PATH):
             lib.nexus_profile_next_call.restype = None
             lib.nexus_debug_force_simt.argtypes = [ctypes.c_int32]
             lib.nexus_debug_force_simt.restype = None
+            lib.nexus_debug_compact_kernel.argtypes = [ctypes.c_int32]
+            lib.nexus_debug_compact_kernel.restype = None
             lib.nexus_debug_scorer_layout.argtypes = [ctypes.c_int32]
             lib.nexus_debug_scorer_layout.restype = None
             lib.nexus_debug_set_trace.argtypes = [ctypes.c_void_p]
@@ -108,6 +110,15 @@ def load(path: str = LIB_PATH):
 def force_simt(on: bool) -> None:
     """Route scoring to the CUDA-core scorer even where the tensor-core one applies."""
     load().nexus_debug_force_simt(1 if on else 0)
+
+
+COMPACT_AUTO, COMPACT_TILES, COMPACT_SLICES = 0, 1, 2
+
+
+def compact_kernel(which: int) -> None:
+    """Testing hook: the compaction kernel, process-wide (COMPACT_TILES, COMPACT_SLICES or
+    COMPACT_AUTO)."""
+    load().nexus_debug_compact_kernel(int(which))
 
 
 def scorer_layout(teams: int) -> None:

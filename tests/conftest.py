@@ -23,3 +23,13 @@ def oracle_lib():
     import oracle
     oracle.build()
     return oracle
+
+
+@pytest.fixture(params=[1, 2], ids=["tiles", "slices"])
+def compact_kernel(request):
+    """Both compaction kernels (the tile kernel and the warp-per-slice one), process-wide
+    for the test, the automatic choice restored afterwards."""
+    from streaming_kv_cache_step_gb300 import nexus
+    nexus.compact_kernel(request.param)
+    yield request.param
+    nexus.compact_kernel(nexus.COMPACT_AUTO)

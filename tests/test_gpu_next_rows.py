@@ -190,7 +190,7 @@ def test_block_select_bitexact_on_oracle_weights(name, mode):
 
 
 @pytest.mark.parametrize("name", list(BLOCKS))
-def test_block_compaction_bitexact_on_oracle_units(name):
+def test_block_compaction_bitexact_on_oracle_units(name, compact_kernel):
     wl = BLOCKS[name]
     run = GpuRun(wl)
     S, cap = run.cache.n_slices, wl.capacity

@@ -156,7 +156,7 @@ def test_select_bitexact_on_oracle_weights(name, mode):
 
 
 @pytest.mark.parametrize("name", list(CASES))
-def test_compact_bitexact_on_oracle_keep(name):
+def test_compact_bitexact_on_oracle_keep(name, compact_kernel):
     wl = CASES[name]
     run = GpuRun(wl)
     S, cap = run.cache.n_slices, wl.capacity
