@@ -82,6 +82,8 @@ WsLayout layout_of(const nx_cache* c, const nx_params* p) {
   o += align_up((size_t)L.slices * 8, 256);
   L.tile_flags = o;
   o += align_up((size_t)L.slices * L.tiles_per_slice * 4, 256);
+  L.select_scratch = o;
+  o += align_up((size_t)(L.slices < kMultiSlices ? L.slices : kMultiSlices) * kMultiStride * 4, 256);
   L.counters_bytes = o - L.counters;
   const size_t cells = (size_t)L.slices * c->capacity;
   L.keys = o;
@@ -242,9 +244,11 @@ nx_status nexus_reservoir_select(const float* w_in, const nx_cache* cache, const
   char* w = static_cast<char*>(ws);
   int32_t* newlen = reinterpret_cast<int32_t*>(w + L.newlen);
   uint32_t* keys = reinterpret_cast<uint32_t*>(w + L.keys);
+  NX_TRY(cudaMemsetAsync(w + L.counters, 0, L.counters_bytes, st));
   NX_TRY(launch_newlen(*cache, *params, newlen, dev_status, st, &launches));
   NX_TRY(launch_keys_from_w(*cache, *params, w_in, keys, newlen, st, &launches));
-  NX_TRY(launch_select(*cache, keys, keep_idx, newlen, params->block_size, st, &launches));
+  NX_TRY(launch_select(*cache, keys, keep_idx, newlen, params->block_size,
+                       reinterpret_cast<int*>(w + L.select_scratch), dev_status, st, &launches));
   return finish(cudaSuccess, launches);
 }
 
@@ -288,7 +292,8 @@ nx_status nexus_evict_step(nx_cache* cache, const void* q, const nx_params* para
   if (params->n_avg > 1)
     NX_TRY(launch_keys_from_w(*cache, *params, reinterpret_cast<const float*>(keys), keys,
                               newlen, st, &launches));
-  NX_TRY(launch_select(*cache, keys, keep, newlen, params->block_size, st, &launches));
+  NX_TRY(launch_select(*cache, keys, keep, newlen, params->block_size,
+                       reinterpret_cast<int*>(w + L.select_scratch), dev_status, st, &launches));
   NX_TRY(launch_compact(*cache, *params, L, w, keep, newlen, dev_status, st, &launches));
   return finish(cudaSuccess, launches);
 }

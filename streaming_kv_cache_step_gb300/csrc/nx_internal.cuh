@@ -22,6 +22,9 @@ constexpr int kMaxPairs = kMaxWalk * (kMaxWalk - 1) / 2;   // walk-row pairs u <
 constexpr int kSimtRows = 256;        // rows per thread block in the CUDA-core scorer
 constexpr int kCompactRows = 32;      // destination rows per compaction tile
 constexpr long long kSpinLimit = 1LL << 22;   // bounded waits: ~0.3-1 s at most
+// the multi-block selection serves up to kMultiSlices slices, kMultiStride ints of scratch each
+constexpr int kMultiSlices = 256;
+constexpr int kMultiStride = 512;
 constexpr uint32_t kForcedKey = 0xFFFFFFFFu;  // order key of a forced (always kept) slot
 
 // ---------------------------------------------------------------------------
@@ -33,6 +36,8 @@ struct WsLayout {
   size_t tile_flags;     // int32 [slices][tiles_per_slice]  (inside counters)
   size_t work;           // int32 [8] global work counters     (inside counters)
   size_t barriers;       // int32 [2][slices] slice arrival counts (inside counters)
+  size_t select_scratch; // int32 [min(slices, kMultiSlices)][kMultiStride] multi-block
+                         // selection scratch (inside counters)
   size_t keys;           // uint32 [slices][capacity] order keys
   size_t stats;          // float [slices][max_chunks][stats_stride] partial softmax stats
   size_t qbar;           // float [slices][W][head_dim] group-mean window queries, or the
@@ -370,8 +375,8 @@ cudaError_t launch_keys_from_w(const nx_cache& c, const nx_params& p, const floa
                                uint32_t* keys, const int32_t* newlen, cudaStream_t st,
                                int* launches);
 cudaError_t launch_select(const nx_cache& c, const uint32_t* keys, int32_t* keep,
-                          const int32_t* newlen, int block_size, cudaStream_t st,
-                          int* launches);
+                          const int32_t* newlen, int block_size, int* scratch,
+                          int32_t* dev_status, cudaStream_t st, int* launches);
 // nx_compact.cu
 cudaError_t launch_newlen(const nx_cache& c, const nx_params& p, int32_t* newlen,
                           int32_t* dev_status, cudaStream_t st, int* launches);

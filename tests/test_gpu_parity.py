@@ -434,6 +434,32 @@ def test_select_reservoir_with_zero_weights_bitexact():
     _select_on_given_weights(TIES, w, nexus.MODE_RESERVOIR)
 
 
+# Few slices longer than one block's shared memory holds (over 48K units, two SMs per
+# slice) take the multi-block selection: every slice split into co-resident segments that
+# merge their digit histograms through global memory. Ragged lengths, a slice within its
+# budget (kept whole), ties at the cutoff, reservoir and top-K.
+MULTI = W.shrink(W.llama3_8b_layer(), seqs=3, kv_heads=2,
+                 lens=np.array([60000, 52222, 800], np.int32), capacity=61440,
+                 budget=np.array([12000, 10444, 900], np.int32), n_hubs=8)
+
+
+@pytest.mark.parametrize("mode", [nexus.MODE_RESERVOIR, nexus.MODE_TOPK])
+def test_select_multi_block_bitexact(mode):
+    rng = np.random.default_rng(31)
+    S, cap = MULTI.n_slices, MULTI.capacity
+    w = (rng.random((S, cap)) * 1e-3 + 1e-6).astype(np.float32)
+    _select_on_given_weights(MULTI, w, mode)
+    assert nexus.last_launch_names()[-1] == "select_multi", nexus.last_launch_names()
+
+
+def test_select_multi_block_heavily_tied_bitexact():
+    rng = np.random.default_rng(32)
+    S, cap = MULTI.n_slices, MULTI.capacity
+    w = (rng.integers(0, 12, (S, cap)) / 5).astype(np.float32)
+    _select_on_given_weights(MULTI, w, nexus.MODE_TOPK)
+    assert nexus.last_launch_names()[-1] == "select_multi", nexus.last_launch_names()
+
+
 @pytest.mark.parametrize("lens,window", [((160_000,), 32), ((170_000, 3000), 32),
                                          ((158_000,), 64), ((157_000,), 16)])
 def test_slices_beyond_the_single_pass_residency_limit(lens, window):
