@@ -27,12 +27,13 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4 raw, float* out) {
   }
 }
 
-// Per-slice validity and new length (blockIdx.y == 0), plus the group-mean window
-// queries: fp32 rows for the CUDA-core scorer (mode 1), or the tensor-core scorer's
+// Per-slice validity and new length, plus the group-mean window queries: fp32 rows for
+// the CUDA-core scorer (mode 1), or the tensor-core scorer's
 // shared-memory image (mode 2): bf16(Qbar) and bf16(Qbar - bf16(Qbar)), each as
 // head_dim/64 column blocks of W rows x 128 bytes in the 128-byte swizzled K-major layout
 // (16-byte chunk c of row n stored at chunk c ^ (n mod 8); 8-row groups 1024 bytes apart).
-// Grid: (slices, W); one thread per pair of adjacent features.
+// Grid: one 256-thread block per slice, or (few slices) up to W 64-thread blocks per
+// slice, block y of a slice taking the window rows n = y mod gridDim.y.
 __global__ void prep_kernel(nx_cache c, const void* __restrict__ q, nx_params p,
                             void* __restrict__ qout, int32_t* __restrict__ newlen,
                             int32_t* dev_status, int mode, int4* __restrict__ counters,
@@ -50,6 +51,7 @@ __global__ void prep_kernel(nx_cache c, const void* __restrict__ q, nx_params p,
   int l, s, h;
   slice_coords(c, slice, l, s, h);
   const int W = p.window, D = c.head_dim, G = c.group;
+  const int ny = gridDim.y;                         // blocks sharing the slice's rows
   if (blockIdx.y == 0) {
     const int T = c.lens[slice];
     __shared__ int bad;
@@ -81,33 +83,60 @@ __global__ void prep_kernel(nx_cache c, const void* __restrict__ q, nx_params p,
       newlen[slice] = bad ? -1 : rows_kept(T, budget_of(p, slice, s), p.block_size);
   }
   if (mode == 0) return;
-  const int n = blockIdx.y;                        // window row
-  const int kk = 2 * threadIdx.x;                  // feature pair
-  if (kk >= D) return;
-  const long long qbase = (((long long)l * c.seqs + s) * (c.kv_heads * (long long)G) +
-                           (long long)h * G) * W * D + (long long)n * D + kk;
-  float v0 = 0.f, v1 = 0.f;
-  for (int g = 0; g < G; ++g) {
-    v0 += ld_elem(q, c.dtype, qbase + (long long)g * W * D);
-    v1 += ld_elem(q, c.dtype, qbase + (long long)g * W * D + 1);
-  }
+  // query head h*G + g belongs to KV head h; the window query is their mean, summed in the
+  // order g = 0, 1, ..., G - 1
+  const long long qslice = (((long long)l * c.seqs + s) * (c.kv_heads * (long long)G) +
+                            (long long)h * G) * W * D;
   const float invG = 1.0f / (float)G;
-  v0 *= invG;
-  v1 *= invG;
-  if (mode == 1) {
-    float* qb = reinterpret_cast<float*>(qout) + ((long long)slice * W + n) * D + kk;
-    qb[0] = v0;
-    qb[1] = v1;
+  if (mode == 2) {
+    // bf16 hi/lo image in the MMA's 128-byte-swizzled K-major layout; 8 features (16 B)
+    // per item, which stay contiguous under the 16-byte swizzle
+    const int KB = D / 64, region = W * 128, groups = D / 8;
+    unsigned char* img = reinterpret_cast<unsigned char*>(qout) + (long long)slice * 2 * KB * region;
+    const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(q);
+    const int rows = (W - (int)blockIdx.y + ny - 1) / ny;     // this block's window rows
+    for (int it = threadIdx.x; it < rows * groups; it += blockDim.x) {
+      const int r = it / groups, kk = (it - r * groups) * 8;
+      const int n = (int)blockIdx.y + r * ny;
+      float v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = 0.f;
+      for (int g = 0; g < G; ++g) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(qb + qslice + (long long)g * W * D +
+                                                           (long long)n * D + kk);
+        const __nv_bfloat162* e2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          v[2 * i] += __low2float(e2[i]);
+          v[2 * i + 1] += __high2float(e2[i]);
+        }
+      }
+      uint4 hw, lw;
+      __nv_bfloat162* hp = reinterpret_cast<__nv_bfloat162*>(&hw);
+      __nv_bfloat162* lp = reinterpret_cast<__nv_bfloat162*>(&lw);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float a0 = v[2 * i] * invG, a1 = v[2 * i + 1] * invG;
+        hp[i] = __floats2bfloat162_rn(a0, a1);
+        lp[i] = __floats2bfloat162_rn(a0 - __low2float(hp[i]), a1 - __high2float(hp[i]));
+      }
+      const int kb = kk >> 6, byte = (kk & 63) * 2;
+      const int off = (n >> 3) * 1024 + (n & 7) * 128 + (((byte >> 4) ^ (n & 7)) << 4);
+      *reinterpret_cast<uint4*>(img + kb * region + off) = hw;
+      *reinterpret_cast<uint4*>(img + (KB + kb) * region + off) = lw;
+    }
     return;
   }
-  const __nv_bfloat162 hi = __floats2bfloat162_rn(v0, v1);
-  const __nv_bfloat162 lo = __floats2bfloat162_rn(v0 - __low2float(hi), v1 - __high2float(hi));
-  const int KB = D / 64, region = W * 128;
-  const int kb = kk >> 6, byte = (kk & 63) * 2;
-  const int off = (n >> 3) * 1024 + (n & 7) * 128 + ((((byte >> 4) ^ (n & 7)) << 4) | (byte & 15));
-  unsigned char* img = reinterpret_cast<unsigned char*>(qout) + (long long)slice * 2 * KB * region;
-  *reinterpret_cast<__nv_bfloat162*>(img + kb * region + off) = hi;
-  *reinterpret_cast<__nv_bfloat162*>(img + (KB + kb) * region + off) = lo;
+  // fp32 group means for the CUDA-core scorer
+  const int rows = (W - (int)blockIdx.y + ny - 1) / ny;
+  for (int it = threadIdx.x; it < rows * D; it += blockDim.x) {
+    const int r = it / D, kk = it - r * D;
+    const int n = (int)blockIdx.y + r * ny;
+    float v = 0.f;
+    for (int g = 0; g < G; ++g)
+      v += ld_elem(q, c.dtype, qslice + (long long)g * W * D + (long long)n * D + kk);
+    reinterpret_cast<float*>(qout)[((long long)slice * W + n) * D + kk] = v * invG;
+  }
 }
 
 template <int N>
@@ -387,9 +416,12 @@ cudaError_t launch_simt_w(const nx_cache& c, const nx_params& p, const WsLayout&
 cudaError_t launch_prep(const nx_cache& c, const void* q, const nx_params& p, const WsLayout& L,
                         char* ws, int32_t* dev_status, cudaStream_t st, int* launches,
                         int mode) {
-  dim3 grid((unsigned)L.slices, mode == 0 ? 1 : p.window);
-  // counters_bytes is a multiple of 64 and the region 256-byte aligned
-  prep_kernel<<<grid, 64, 0, st>>>(c, q, p, ws + L.qbar,
+  // few slices: spread each slice's window rows over several blocks
+  const int ny = L.slices >= 1024 ? 1 : (int)min((long long)p.window, (1024 + L.slices - 1) / L.slices);
+  dim3 grid((unsigned)L.slices, (unsigned)(mode == 0 ? 1 : ny));
+  // counters_bytes is a multiple of 64 and the region 256-byte aligned; a block that takes
+  // a few rows of its slice needs fewer threads
+  prep_kernel<<<grid, grid.y > 1 ? 64 : 256, 0, st>>>(c, q, p, ws + L.qbar,
                                    reinterpret_cast<int32_t*>(ws + L.newlen), dev_status, mode,
                                    reinterpret_cast<int4*>(ws + L.counters),
                                    (long long)(L.counters_bytes / 16));
