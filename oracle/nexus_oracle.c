@@ -25,7 +25,8 @@
  * Readings where §2.1-§2.3 leave a detail unstated (each the plainest reading of the
  * surrounding text):
  *   block size b = 1 (BlockSum and rownorm are identities); the window query Q
- *   is the mean of the G query heads that share the KV head; no causal mask;
+ *   is the mean of the G query heads that share the KV head, in the model's dtype
+ *   (for a bf16 cache: the mean rounded once to bf16); no causal mask;
  *   the walk uses the last H window rows oldest first, without damping, and
  *   c~ = 0 when H = 0; forced slots are the first n_sink and the last n_recent
  *   slots; ties in the key are broken by the larger slot (the newer token).
@@ -60,6 +61,17 @@ static double nxo_bf16_to_double(uint16_t h) {
 static double nxo_load(const void* base, int dtype, int64_t idx) {
   if (dtype == NXO_BF16) return nxo_bf16_to_double(((const uint16_t*)base)[idx]);
   return (double)((const float*)base)[idx];
+}
+
+/* bfloat16 rounding of a double: to the nearest value with 8 significant bits (binary32's
+ * exponent range, so below 2^-126 to a multiple of 2^-133), ties to even. Finite inputs
+ * within the bf16 range only. */
+static double nxo_round_bf16(double x) {
+  if (x == 0.0 || !isfinite(x)) return x;
+  if (fabs(x) < ldexp(1.0, -126)) return ldexp(nearbyint(ldexp(x, 133)), -133);
+  int e;
+  const double m = frexp(x, &e);            /* x = m 2^e, 0.5 <= |m| < 1 */
+  return ldexp(nearbyint(ldexp(m, 8)), e - 8);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -567,7 +579,8 @@ int nxo_evict_step(nxo_cache* c, const void* q, const nxo_params* p, int n_sel,
       }
       /* a unit's position is that of its first slot */
       for (int u = 0; u < N; ++u) pj[u] = c->pos[nxo_row(c, l, s, h, u * bs)];
-      /* The window query of the KV group: mean of its G query heads. */
+      /* The window query of the KV group: mean of its G query heads, a tensor of the
+       * model's dtype (a bf16 model's head average is bf16: the mean rounded once). */
       for (int w_ = 0; w_ < W; ++w_)
         for (int k = 0; k < d; ++k) {
           double acc = 0.0;
@@ -576,7 +589,8 @@ int nxo_evict_step(nxo_cache* c, const void* q, const nxo_params* p, int n_sel,
             int64_t idx = ((((int64_t)l * S + s) * (Hk * G) + hq) * W + w_) * d + k;
             acc += nxo_load(q, c->dtype, idx);
           }
-          Qb[(size_t)w_ * d + k] = acc / (double)G;
+          const double mean = acc / (double)G;
+          Qb[(size_t)w_ * d + k] = c->dtype == NXO_BF16 ? nxo_round_bf16(mean) : mean;
         }
       int rc = 0, nk = 0;
       if (T > 0) {

@@ -41,7 +41,7 @@ struct WsLayout {
   size_t keys;           // uint32 [slices][capacity] order keys
   size_t stats;          // float [slices][max_chunks][stats_stride] partial softmax stats
   size_t qbar;           // float [slices][W][head_dim] group-mean window queries, or the
-                         // tensor-core scorer's bf16 hi/lo image of the same size
+                         // tensor-core scorer's bf16 image (half the size)
   size_t newlen;         // int32 [slices]
   size_t keep;           // int32 [slices][capacity] kept slots (when the caller gives none)
   size_t total;

@@ -27,10 +27,11 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4 raw, float* out) {
   }
 }
 
-// Per-slice validity and new length, plus the group-mean window queries: fp32 rows for
-// the CUDA-core scorer (mode 1), or the tensor-core scorer's
-// shared-memory image (mode 2): bf16(Qbar) and bf16(Qbar - bf16(Qbar)), each as
-// head_dim/64 column blocks of W rows x 128 bytes in the 128-byte swizzled K-major layout
+// Per-slice validity and new length, plus the group-mean window queries Qbar, a tensor of
+// the model's dtype (for bf16 caches the mean rounded once to bf16, as a bf16 model's head
+// average is): fp32 rows for the CUDA-core scorer (mode 1), or the tensor-core scorer's
+// shared-memory image (mode 2) of the bf16 Qbar as head_dim/64 column blocks of W rows x
+// 128 bytes in the 128-byte swizzled K-major layout
 // (16-byte chunk c of row n stored at chunk c ^ (n mod 8); 8-row groups 1024 bytes apart).
 // Grid: one 256-thread block per slice, or (few slices) up to W 64-thread blocks per
 // slice, block y of a slice taking the window rows n = y mod gridDim.y.
@@ -89,10 +90,10 @@ __global__ void prep_kernel(nx_cache c, const void* __restrict__ q, nx_params p,
                             (long long)h * G) * W * D;
   const float invG = 1.0f / (float)G;
   if (mode == 2) {
-    // bf16 hi/lo image in the MMA's 128-byte-swizzled K-major layout; 8 features (16 B)
-    // per item, which stay contiguous under the 16-byte swizzle
+    // the bf16 image in the MMA's 128-byte-swizzled K-major layout; 8 features (16 B) per
+    // item, which stay contiguous under the 16-byte swizzle
     const int KB = D / 64, region = W * 128, groups = D / 8;
-    unsigned char* img = reinterpret_cast<unsigned char*>(qout) + (long long)slice * 2 * KB * region;
+    unsigned char* img = reinterpret_cast<unsigned char*>(qout) + (long long)slice * KB * region;
     const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(q);
     const int rows = (W - (int)blockIdx.y + ny - 1) / ny;     // this block's window rows
     for (int it = threadIdx.x; it < rows * groups; it += blockDim.x) {
@@ -111,23 +112,17 @@ __global__ void prep_kernel(nx_cache c, const void* __restrict__ q, nx_params p,
           v[2 * i + 1] += __high2float(e2[i]);
         }
       }
-      uint4 hw, lw;
+      uint4 hw;
       __nv_bfloat162* hp = reinterpret_cast<__nv_bfloat162*>(&hw);
-      __nv_bfloat162* lp = reinterpret_cast<__nv_bfloat162*>(&lw);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float a0 = v[2 * i] * invG, a1 = v[2 * i + 1] * invG;
-        hp[i] = __floats2bfloat162_rn(a0, a1);
-        lp[i] = __floats2bfloat162_rn(a0 - __low2float(hp[i]), a1 - __high2float(hp[i]));
-      }
+      for (int i = 0; i < 4; ++i) hp[i] = __floats2bfloat162_rn(v[2 * i] * invG, v[2 * i + 1] * invG);
       const int kb = kk >> 6, byte = (kk & 63) * 2;
       const int off = (n >> 3) * 1024 + (n & 7) * 128 + (((byte >> 4) ^ (n & 7)) << 4);
       *reinterpret_cast<uint4*>(img + kb * region + off) = hw;
-      *reinterpret_cast<uint4*>(img + (KB + kb) * region + off) = lw;
     }
     return;
   }
-  // fp32 group means for the CUDA-core scorer
+  // group means as fp32 rows for the CUDA-core scorer (bf16 caches: the bf16 mean)
   const int rows = (W - (int)blockIdx.y + ny - 1) / ny;
   for (int it = threadIdx.x; it < rows * D; it += blockDim.x) {
     const int r = it / D, kk = it - r * D;
@@ -135,7 +130,9 @@ __global__ void prep_kernel(nx_cache c, const void* __restrict__ q, nx_params p,
     float v = 0.f;
     for (int g = 0; g < G; ++g)
       v += ld_elem(q, c.dtype, qslice + (long long)g * W * D + (long long)n * D + kk);
-    reinterpret_cast<float*>(qout)[((long long)slice * W + n) * D + kk] = v * invG;
+    const float m = v * invG;
+    reinterpret_cast<float*>(qout)[((long long)slice * W + n) * D + kk] =
+        c.dtype == NX_DTYPE_BF16 ? __bfloat162float(__float2bfloat16_rn(m)) : m;
   }
 }
 

@@ -8,10 +8,9 @@
 //   1. a TMA producer thread stages each K tile in a ring of shared-memory stages
 //      (128-byte swizzle, one box per 64-element column block -- per page when paged);
 //   2. an MMA thread issues tcgen05.mma (kind::f16, bf16 x bf16 -> fp32), M = 128 rows,
-//      N = W window rows, K = head_dim, twice: against bf16(Qbar) and against
-//      bf16(Qbar - bf16(Qbar)), accumulating in the same TMEM columns, so the logits keep
-//      fp32 accuracy although the tensor cores take bf16 operands. A chunk's logits fill
-//      one of two or three TMEM buffers (tile t -> columns [t*W, (t+1)*W));
+//      N = W window rows, K = head_dim, against Qbar -- a bf16 tensor, the head average of
+//      a bf16 model -- so the logits are the exact products summed in fp32. A chunk's
+//      logits fill one of two or three TMEM buffers (tile t -> columns [t*W, (t+1)*W));
 //   3. the epilogue warpgroups (one TMEM lane = one row) take per-column maxima over each
 //      warp's rows, write e = exp((l - max)/sqrt(d)) back to TMEM, and store the chunk
 //      record (chunk maxima, sums, the H x H Gram of the walk rows); a publisher warp
@@ -67,7 +66,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 struct Args {
   nx_cache c;
   nx_params p;
-  const unsigned char* qimg;   // [slices] shared-memory images of bf16 hi/lo queries
+  const unsigned char* qimg;   // [slices] shared-memory images of the bf16 window queries
   uint32_t tmem_cols;      // columns the CTA allocates (all 512; split between its teams)
   int nbuf;                // TMEM buffers (2: the next chunk's MMAs overlap this epilogue)
   long long* trace;        // optional phase trace: [grid][kTraceEvents][2] (null: off)
@@ -326,7 +325,7 @@ struct Smem {
   static constexpr int kRegionA = kTileRows * 128;        // one column block of a K tile
   static constexpr int kTileBytes = KB * kRegionA;
   static constexpr int kRegionB = W * 128;                // one column block of Qbar
-  static constexpr int kQBytes = 2 * KB * kRegionB;       // hi + lo query image
+  static constexpr int kQBytes = KB * kRegionB;           // bf16 query image
   static constexpr int kRec = 2 * W + kMaxPairs;          // floats of one chunk record
   static constexpr int kRedStride = W + kMaxPairs;        // one warp's partial reductions
   static constexpr int kOffK = 0;
@@ -1482,15 +1481,12 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Args A) {
           const uint32_t ka = smem_u32(sm + S::kOffK + st * S::kTileBytes);
           const uint32_t dt = tmem + b * buf_cols + (uint32_t)(t * W);
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
+          for (int kb = 0; kb < S::KB; ++kb) {
 #pragma unroll
-            for (int kb = 0; kb < S::KB; ++kb) {
-#pragma unroll
-              for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t da = sw128_desc(ka + kb * S::kRegionA + ks * 32);
-                const uint64_t db = sw128_desc(qa + (half * S::KB + kb) * S::kRegionB + ks * 32);
-                mma_bf16(dt, da, db, kIdesc, (half | kb | ks) ? 1u : 0u);
-              }
+            for (int ks = 0; ks < 4; ++ks) {
+              const uint64_t da = sw128_desc(ka + kb * S::kRegionA + ks * 32);
+              const uint64_t db = sw128_desc(qa + kb * S::kRegionB + ks * 32);
+              mma_bf16(dt, da, db, kIdesc, (kb | ks) ? 1u : 0u);
             }
           }
           mma_commit(&bar_empty[st]);      // the stage's smem is free once these finish

@@ -13,6 +13,14 @@ DEV = "cuda:0"
 RTOL = 1e-3           # scores: bf16 inputs, fp32 accumulation, vs the fp64 oracle
 
 
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """The window query of a bf16 model is bf16: round (through binary32) to the nearest
+    bfloat16, ties to even, by the bit-level rule; returns float64."""
+    b = np.asarray(x, np.float64).astype(np.float32).view(np.uint32).astype(np.uint64)
+    b = ((b + 0x7FFF + ((b >> 16) & 1)) >> 16) << 16
+    return b.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
 def score_tol(ref: np.ndarray, T: int) -> np.ndarray:
     """|gpu - oracle| bound per entry: rtol 1e-3, plus 1e-3/T absolute for entries near 0."""
     return RTOL * np.abs(ref) + 1e-3 / max(T, 1)

@@ -12,8 +12,8 @@ import pytest
 import torch
 
 import oracle
-from harness import (DEV, GpuRun, compare_survivors, oracle_kappa, oracle_slice, score_tol,
-                     slice_budget)
+from harness import (DEV, GpuRun, compare_survivors, oracle_kappa, oracle_slice, round_bf16,
+                     score_tol, slice_budget)
 from streaming_kv_cache_step_gb300 import nexus
 from streaming_kv_cache_step_gb300 import workloads as W
 
@@ -175,6 +175,8 @@ def test_block_scores_match_oracle(name):
             k = (k.astype(np.uint32) << 16).view(np.float32)
             q = (q.astype(np.uint32) << 16).view(np.float32)
         Qb = q.reshape(wl.group, wl.window, wl.head_dim).astype(np.float64).mean(0)
+        if wl.dtype == "bf16":
+            Qb = round_bf16(Qb)             # a bf16 model's head average is bf16
         o = oracle.block_scores(k.astype(np.float64), Qb, wl.walk_len, 32, wl.lam, wl.eps_tie)
         assert np.all(np.abs(a[sid, :N] - o["a"]) <= score_tol(o["a"], N)), sid
         assert np.all(np.abs(w[sid, :N] - ref["w"][0, :N]) <= score_tol(ref["w"][0, :N], N))

@@ -6,7 +6,8 @@ import pytest
 import torch
 
 import oracle
-from harness import (DEV, GpuRun, compare_survivors, oracle_kappa, oracle_slice, score_tol)
+from harness import (DEV, GpuRun, compare_survivors, oracle_kappa, oracle_slice, round_bf16,
+                     score_tol)
 from streaming_kv_cache_step_gb300 import nexus
 from streaming_kv_cache_step_gb300 import workloads as W
 
@@ -100,6 +101,8 @@ def _decode(c, q, wl):
     else:
         qf = q
     qbar = qf.reshape(wl.group, wl.window, wl.head_dim).astype(np.float64).mean(0)
+    if k.dtype == np.float32 and wl.dtype == "bf16":
+        qbar = round_bf16(qbar)         # a bf16 model's head average is bf16
     return k.astype(np.float64), qbar
 
 

@@ -3,7 +3,9 @@ sequence, KV head) slice of a cache) against its single-slice pieces, fed by han
 
 * the window query of a KV group is the mean of that group's G query heads (Nexus
   Sampling paper, §2.1: the window queries are "head-averaged representations";
-  query head h*G + g belongs to KV head h);
+  query head h*G + g belongs to KV head h), in the model's dtype: for a bf16 cache the
+  mean rounded once to bf16 (here by a float32 bit-level rounding written
+  independently of the oracle's);
 * the Philox stream of a slice is indexed by head id (layer_id_base + l)*Hkv + h and
   sequence id seq_id_base + s (§2.3: the uniforms u_j of Eq. (6) are independent
   per candidate, so every slice draws from its own stream);
@@ -106,8 +108,11 @@ def test_group_mean_query_and_slice_scores(oracle_lib, dtype):
         h, s, l = sid % HKV, (sid // HKV) % S, sid // (HKV * S)
         T = int(LENS[s])
         K = dec(cache["k"][l, s, h, :T])
-        # KV head h owns query heads h*G .. h*G + G - 1; its window query is their mean
+        # KV head h owns query heads h*G .. h*G + G - 1; its window query is their mean,
+        # a tensor of the model's dtype (bf16: the mean rounded once to bf16)
         Qbar = dec(q[l, s, h * G:(h + 1) * G]).mean(axis=0)
+        if dtype == "bf16":
+            Qbar = _decode(_bf16_bits(Qbar))
         o = oracle_lib.slice_scores(K, Qbar, H, 0.5, 1e-6)
         # the same additions in the same order: bit-equal
         assert np.array_equal(out["a"][sid, :T], o["a"]), sid
