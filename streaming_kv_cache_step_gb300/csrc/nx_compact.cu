@@ -312,9 +312,13 @@ cudaError_t launch_slices(const nx_cache& c, const int32_t* keep, const int32_t*
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, compact_slices_kernel<CH>,
                                                 kCompactThreads, 0);
   constexpr int kWarps = kCompactThreads / 32;
-  long long grid = (long long)sms * (per_sm > 0 ? per_sm : 1);
-  const long long need = (slices + kWarps - 1) / kWarps;
-  if (grid > need) grid = need;
+  // as many warps as fit, but the same number of slices for each: with k slices per warp
+  // at most, ceil(slices / k) warps (a warp with one slice more than the others would set
+  // the kernel's time alone)
+  const long long fit = (long long)sms * (per_sm > 0 ? per_sm : 1) * kWarps;
+  const long long k = (slices + fit - 1) / fit;
+  const long long warps = (slices + k - 1) / k;
+  long long grid = (warps + kWarps - 1) / kWarps;
   if (grid < 1) grid = 1;
   return launch_after(compact_slices_kernel<CH>, dim3((unsigned)grid), dim3(kCompactThreads),
                       0, st, c, keep, newlen, slices, bs);
