@@ -63,6 +63,7 @@ def _load():
             lib.nxo_exp_spec.argtypes = [ctypes.c_float]
             lib.nxo_exp_spec.restype = ctypes.c_float
             lib.nxo_exp_spec_many.argtypes = [ctypes.c_int64, c_p, c_p]
+            lib.nxo_round_bf16_many.argtypes = [ctypes.c_int64, c_p, c_p]
             lib.nxo_block_scores.argtypes = ([ctypes.c_int] * 5 + [ctypes.c_double] * 2
                                              + [c_p] * 8)
             lib.nxo_block_scores.restype = ctypes.c_int
@@ -179,6 +180,16 @@ def exp_spec(x):
     x = np.ascontiguousarray(x, dtype=np.float32)
     o = np.zeros_like(x)
     lib.nxo_exp_spec_many(x.size, _ptr(x), _ptr(o))
+    return o
+
+
+def round_bf16(x):
+    """The window queries of a bf16 model as the oracle forms them: each value rounded to
+    the nearest bfloat16 (ties to even), elementwise over a float64 array."""
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    o = np.zeros_like(x)
+    lib.nxo_round_bf16_many(x.size, _ptr(x), _ptr(o))
     return o
 
 

@@ -357,6 +357,11 @@ float nxo_exp_spec(float x) {
   return p * scale;
 }
 
+/* bfloat16 rounding of the window queries (the model's dtype), elementwise over doubles. */
+void nxo_round_bf16_many(int64_t n, const double* x, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = nxo_round_bf16(x[i]);
+}
+
 void nxo_exp_spec_many(int64_t n, const float* x, float* out) {
   for (int64_t i = 0; i < n; ++i) out[i] = nxo_exp_spec(x[i]);
 }

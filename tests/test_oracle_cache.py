@@ -203,3 +203,23 @@ def test_paged_compaction_moves_the_kept_rows(oracle_lib):
     # the block table is not modified and pages outside every table are untouched
     unused = np.setdiff1d(np.arange(paged["num_pages"]), bt.reshape(-1))
     assert np.array_equal(paged["k"][:, unused], before["k"][:, unused])
+
+
+def test_bf16_rounding_of_the_window_queries(oracle_lib):
+    # the oracle's rounding of the head average (to 8 significant bits, ties to even,
+    # binary32's exponent range) against the bit-level rule on binary32 inputs: random
+    # values, exact halfway cases either side of even, subnormals, and the float32 range
+    rng = np.random.default_rng(7)
+    x = np.concatenate([rng.standard_normal(20000) * 3,
+                        rng.standard_normal(2000) * 1e-30,
+                        rng.standard_normal(2000) * 1e-39,            # binary32 subnormals
+                        rng.standard_normal(2000) * 1e30]).astype(np.float32)
+    base = _bf16_bits(rng.standard_normal(4000).astype(np.float32))
+    half = ((base.astype(np.uint32) << 16) | 0x8000).view(np.float32)  # exactly between two
+    x = np.concatenate([x, half, -half, np.float32([0.0, -0.0, 1.0, 65504.0])])
+    got = oracle_lib.round_bf16(x.astype(np.float64))
+    want = _decode(_bf16_bits(x))
+    assert np.array_equal(got, want)
+    # ties went to the even neighbour, so a halfway value never rounds the same way twice
+    ev = _bf16_bits(half)
+    assert ((ev & 1) == 0).all()
